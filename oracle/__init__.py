@@ -1,0 +1,31 @@
+"""CPU oracle for the zero-copy MoE route -> dispatch -> expert -> combine path.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the benchmark's CPU-baseline / reference arm may import or run anything in
+this package.  The product path (the CUDA library and its Python binding)
+never imports it and has no CPU fallback.
+
+The oracle is a plain, slow, obviously-correct numpy implementation in fp64 of
+what the path computes (module ``oracle.moe``).  It shares no code with the
+CUDA path; both take their inputs from the seeded generator module
+``moe_synth``.
+
+Parity pins: every function here is pinned by ``tests/test_oracle_*.py``
+against brute force on tiny inputs, closed forms, invariants and a
+hand-worked example under ``tests/golden/``.  The end-to-end float values have
+no printed worked example in the source pages, so beyond those closed forms
+and invariants their absolute values are parity-unpinned.
+"""
+from .moe import (  # noqa: F401
+    bf16_bits_to_f64,
+    round_f64_to_bf16_bits,
+    route_topk,
+    count_experts,
+    place_pairs,
+    dispatch_rows,
+    expert_ffn_rows,
+    expert_ffn,
+    combine,
+    pipeline,
+    slot_address,
+)

@@ -1,0 +1,279 @@
+"""Pins of the CPU oracle against things other than itself: brute force on tiny
+inputs, closed forms, invariants, a hand-worked example (tests/golden/) and
+an independent library implementation (torch CPU) of the expert FFN."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_synth as ms
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# --------------------------------------------------------------- bf16 helpers
+
+def test_bf16_round_trip_and_ties():
+    assert oracle.bf16_bits_to_f64(np.array([0x3F80]))[0] == 1.0
+    assert oracle.bf16_bits_to_f64(np.array([0x4049]))[0] == 3.140625
+    assert oracle.bf16_bits_to_f64(np.array([0xC000]))[0] == -2.0
+    v = np.array([1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, -2.0, 3.390625, 1 + 2 ** -8 + 2 ** -20,
+                  1 + 2 ** -8 + 2 ** -30])
+    got = oracle.round_f64_to_bf16_bits(v).tolist()
+    # 1+2^-8 is half-way between 0x3F80 and 0x3F81: ties to even -> 0x3F80;
+    # 1+3*2^-8 is half-way between 0x3F81 and 0x3F82 -> 0x3F82; just above the
+    # first tie (by an fp32-representable 2^-20) it rounds up -> 0x3F81.  The
+    # stated rounding goes through fp32 (as an fp32 accumulator does), so an
+    # excess of 2^-30, below half an fp32 ulp, is lost first and the tie rule
+    # applies -> 0x3F80.
+    assert got == [0x3F80, 0x3F80, 0x3F82, 0xC000, 0x4059, 0x3F81, 0x3F80]
+
+
+# --------------------------------------------------------------- address
+
+def test_peer_address_golden():
+    g = _golden("peer_address.json")
+    for c in g["cases"]:
+        stride = c["stride4G"] << 32
+        got = oracle.slot_address(int(c["win_base"], 16), c["peer"], stride, int(c["offset"], 16))
+        assert got == int(c["expect"], 16)
+
+
+# --------------------------------------------------------------- routing
+
+def _brute_topk(lg, k):
+    n, e = lg.shape
+    out = np.zeros((n, k), dtype=np.int64)
+    for g in range(n):
+        for a in range(e):
+            rank = sum(1 for b in range(e) if lg[g, b] > lg[g, a] or (lg[g, b] == lg[g, a] and b < a))
+            if rank < k:
+                out[g, rank] = a
+    return out
+
+
+@pytest.mark.parametrize("e,k", [(4, 2), (8, 2), (16, 8), (16, 1), (9, 3)])
+def test_route_brute_force_with_ties(e, k):
+    rng = np.random.default_rng(e * 10 + k)
+    # coarse quantisation makes ties frequent
+    lg = (np.round(rng.standard_normal((64, e)) * 2) / 2).astype(np.float32)
+    idx, w = oracle.route_topk(lg, k)
+    assert np.array_equal(idx, _brute_topk(lg, k))
+    for g in range(64):
+        sel = [float(lg[g, i]) for i in idx[g]]
+        for j in range(k):
+            ref = 1.0 / sum(math.exp(s - sel[j]) for s in sel)
+            assert abs(float(w[g, j]) - ref) <= 1e-6 * max(1.0, ref)
+    assert np.all(np.abs(w.astype(np.float64).sum(1) - 1.0) <= 1e-6)
+    assert all(len(set(r)) == k for r in idx.tolist())
+
+
+@pytest.mark.parametrize("k", [1, 2, 4, 8])
+def test_route_all_equal(k):
+    lg = np.full((5, 16), 0.25, dtype=np.float32)
+    idx, w = oracle.route_topk(lg, k)
+    assert np.array_equal(idx, np.tile(np.arange(k), (5, 1)))
+    assert np.all(w == np.float32(1.0 / k))
+
+
+def test_route_k1_weight_is_one():
+    lg = ms.logits_np(ms.CONFIGS["tiny"])
+    idx, w = oracle.route_topk(lg, 1)
+    assert np.all(w == 1.0)
+    assert np.array_equal(idx[:, 0], np.argmax(lg, axis=1))
+
+
+def test_route_hand_golden():
+    g = _golden("dispatch_hand.json")
+    idx, w = oracle.route_topk(np.array(g["logits"], dtype=np.float32), g["topk"])
+    assert idx.tolist() == g["idx"]
+    assert np.allclose(w, np.array(g["w"]), rtol=0, atol=1e-7)
+
+
+# --------------------------------------------------------------- count / place
+
+def test_place_hand_golden():
+    g = _golden("dispatch_hand.json")
+    idx = np.array(g["idx"])
+    w = np.array(g["w"], dtype=np.float32)
+    cnt, off, tot = oracle.count_experts(idx, g["num_experts"], g["world"])
+    assert cnt.tolist() == g["cnt"] and off.tolist() == g["recv_off"] and tot.tolist() == g["total_recv"]
+    pos, rp, rw = oracle.place_pairs(idx, w, g["num_experts"], g["world"])
+    assert pos.tolist() == g["pos"]
+    assert [r.tolist() for r in rp] == g["recv_pair"]
+    assert rw[1][0] == w[0, 1] and rw[0][0] == w[1, 0]
+
+
+def _random_routing(n, e, k, seed):
+    rng = np.random.default_rng(seed)
+    lg = rng.standard_normal((n, e)).astype(np.float32)
+    return oracle.route_topk(lg, k)
+
+
+@pytest.mark.parametrize("n,e,w,k", [(40, 8, 2, 2), (33, 16, 4, 3), (24, 4, 4, 1), (30, 12, 3, 4)])
+def test_place_brute_force_and_invariants(n, e, w, k):
+    idx, wt = _random_routing(n, e, k, n + e)
+    cnt, off, tot = oracle.count_experts(idx, e, w)
+    e_loc = e // w
+    assert cnt.sum() == n * k
+    for d in range(w):
+        local = cnt[d * e_loc:(d + 1) * e_loc]
+        assert np.array_equal(off[d * e_loc:(d + 1) * e_loc], np.concatenate([[0], np.cumsum(local)[:-1]]))
+        assert tot[d] == local.sum()
+    pos, rp, _ = oracle.place_pairs(idx, wt, e, w)
+    flat = idx.reshape(-1)
+    for p in range(n * k):
+        ex = int(flat[p])
+        before = int(np.sum(flat[:p] == ex))        # O(P^2) independent count
+        assert pos.reshape(-1)[p] == off[ex] + before
+    # bijection: every row [0, total_recv[d]) of every slot is hit exactly once
+    seen = [np.zeros(int(tot[d]), dtype=np.int64) for d in range(w)]
+    for g in range(n):
+        for j in range(k):
+            d = int(idx[g, j]) // e_loc
+            seen[d][pos[g, j]] += 1
+            assert rp[d][pos[g, j]] == g * k + j
+    assert all(np.all(s == 1) for s in seen)
+
+
+def test_place_receive_order_is_slot_token_k():
+    # tokens 0..T-1 live on slot 0, T..2T-1 on slot 1; inside one expert the
+    # received rows must be ordered by (source slot, token, k)
+    idx, wt = _random_routing(64, 4, 2, 7)
+    pos, rp, _ = oracle.place_pairs(idx, wt, 4, 2)
+    cnt, off, _ = oracle.count_experts(idx, 4, 2)
+    for e in range(4):
+        d = e // 2
+        pairs = rp[d][off[e]:off[e] + cnt[e]]
+        assert np.all(np.diff(pairs) > 0)
+
+
+def test_dispatch_rows_are_bit_copies():
+    cfg = ms.CONFIGS["tiny"]
+    x = ms.x_np(cfg)
+    idx, w = oracle.route_topk(ms.logits_np(cfg), cfg["topk"])
+    pos, rp, _ = oracle.place_pairs(idx, w, cfg["num_experts"], cfg["world"])
+    rx = oracle.dispatch_rows(x, rp, cfg["topk"])
+    e_loc = cfg["num_experts"] // cfg["world"]
+    for g in range(x.shape[0]):
+        for j in range(cfg["topk"]):
+            assert np.array_equal(rx[int(idx[g, j]) // e_loc][pos[g, j]], x[g])
+
+
+# --------------------------------------------------------------- FFN
+
+def _bits(a):
+    return ms.f32_to_bf16_bits_np(np.asarray(a, dtype=np.float32))
+
+
+def test_ffn_zero_up_gives_zero():
+    rng = np.random.default_rng(1)
+    a = _bits(rng.standard_normal((5, 16)))
+    wg = _bits(rng.standard_normal((8, 16)) * 0.1)
+    wu = np.zeros((8, 16), dtype=np.uint16)
+    wd = _bits(rng.standard_normal((16, 8)) * 0.1)
+    h, y, ye = oracle.expert_ffn_rows(a, wg, wu, wd)
+    assert np.all(oracle.bf16_bits_to_f64(h) == 0) and np.all(oracle.bf16_bits_to_f64(y) == 0)
+
+
+def integer_ffn_case(rows, hidden, inter):
+    """One-hot rows, small-integer weights with gate >= 32 so that silu(gate)
+    equals gate after rounding to fp32; every product and sum is an exact
+    small integer, so h and y have closed forms."""
+    a = np.zeros((rows, hidden), dtype=np.float32)
+    col = [(3 * r + 1) % hidden for r in range(rows)]
+    for r in range(rows):
+        a[r, col[r]] = 1.0
+    wg = np.zeros((inter, hidden), dtype=np.float32)
+    wu = np.zeros((inter, hidden), dtype=np.float32)
+    for i in range(inter):
+        for c in range(hidden):
+            wg[i, c] = 32 + (i + 2 * c) % 5
+            wu[i, c] = ((i * 7 + c) % 5) - 2
+    wd = np.zeros((hidden, inter), dtype=np.float32)
+    for o in range(hidden):
+        wd[o, (5 * o + 3) % inter] = 1.0
+        wd[o, (o + 1) % inter] = -1.0 if (o + 1) % inter != (5 * o + 3) % inter else 0.0
+    h = np.zeros((rows, inter))
+    for r in range(rows):
+        c = col[r]
+        for i in range(inter):
+            h[r, i] = (32 + (i + 2 * c) % 5) * (((i * 7 + c) % 5) - 2)
+    y = np.zeros((rows, hidden))
+    for r in range(rows):
+        for o in range(hidden):
+            y[r, o] = sum(h[r, i] * wd[o, i] for i in range(inter) if wd[o, i] != 0)
+    return _bits(a), _bits(wg), _bits(wu), _bits(wd), h, y
+
+
+def test_ffn_integer_closed_form():
+    a, wg, wu, wd, h_ref, y_ref = integer_ffn_case(6, 24, 40)
+    h, y, ye = oracle.expert_ffn_rows(a, wg, wu, wd)
+    assert np.array_equal(oracle.bf16_bits_to_f64(h), h_ref)
+    assert np.array_equal(oracle.bf16_bits_to_f64(y), y_ref)
+
+
+def test_ffn_matches_torch_cpu_fp32():
+    cfg = ms.CONFIGS["tiny"]
+    x = ms.x_np(cfg)[:40]
+    wg, wu, wd = (ms.weight_np(cfg, n, 1) for n in ("gate", "up", "down"))
+    h, y, ye = oracle.expert_ffn_rows(x, wg, wu, wd)
+    t = lambda b: torch.from_numpy(oracle.bf16_bits_to_f64(b).astype(np.float32))
+    ht = torch.nn.functional.silu(t(x) @ t(wg).T) * (t(x) @ t(wu).T)
+    yt = ht @ t(wd).T
+    assert torch.allclose(torch.from_numpy(oracle.bf16_bits_to_f64(h)).float(), ht, rtol=1e-2, atol=1e-3)
+    rel = np.linalg.norm(ye - yt.double().numpy()) / np.linalg.norm(yt.double().numpy())
+    assert rel < 1e-2
+    # a transposed or swapped operand would be far off
+    bad = (torch.nn.functional.silu(t(x) @ t(wu).T) * (t(x) @ t(wg).T)) @ t(wd).T
+    assert np.linalg.norm(ye - bad.double().numpy()) / np.linalg.norm(bad.double().numpy()) > 0.1
+
+
+# --------------------------------------------------------------- combine
+
+def test_combine_hand_golden():
+    g = _golden("dispatch_hand.json")
+    y = [_bits(np.array(v, dtype=np.float32)) for v in g["y"]]
+    out = oracle.combine(y, np.array(g["idx"]), np.array(g["w"], dtype=np.float32),
+                         np.array(g["pos"]), g["num_experts"], g["world"])
+    assert oracle.bf16_bits_to_f64(out).tolist() == g["out"]
+
+
+def test_combine_k1_is_the_row():
+    rng = np.random.default_rng(3)
+    idx, w = _random_routing(20, 4, 1, 5)
+    pos, rp, _ = oracle.place_pairs(idx, w, 4, 2)
+    _, _, tot = oracle.count_experts(idx, 4, 2)
+    y = [_bits(rng.standard_normal((int(tot[d]), 8))) for d in range(2)]
+    out = oracle.combine(y, idx, w, pos, 4, 2)
+    for g in range(20):
+        assert np.array_equal(out[g], y[int(idx[g, 0]) // 2][pos[g, 0]])
+
+
+# --------------------------------------------------------------- whole path
+
+def test_pipeline_tiny_consistency():
+    cfg = ms.CONFIGS["tiny"]
+    res = oracle.pipeline(ms.logits_np(cfg), ms.x_np(cfg), cfg,
+                          lambda e: tuple(ms.weight_np(cfg, n, e) for n in ("gate", "up", "down")))
+    n, k = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"]
+    assert res["cnt"].sum() == n * k
+    assert res["out"].shape == (n, cfg["hidden"])
+    # out equals the weighted sum of per-token FFN rows computed token by token
+    for g in (0, 17, 127):
+        acc = np.zeros(cfg["hidden"])
+        for j in range(k):
+            e = int(res["idx"][g, j])
+            wts = tuple(ms.weight_np(cfg, nm, e) for nm in ("gate", "up", "down"))
+            _, yb, _ = oracle.expert_ffn_rows(ms.x_np(cfg, rows=[g]), *wts)
+            acc += float(res["w"][g, j]) * oracle.bf16_bits_to_f64(yb[0])
+        assert np.array_equal(res["out"][g], oracle.round_f64_to_bf16_bits(acc))
