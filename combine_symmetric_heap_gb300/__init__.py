@@ -1,0 +1,279 @@
+"""Zero-copy MoE dispatch -> expert -> combine over a flat symmetric heap, GB300.
+
+Thin Python binding of the C-ABI library ``libsymmoe.so`` (declared in
+``include/symmoe.h``).  Functions keep the C names and only marshal
+arguments: torch tensors or raw device addresses in, ``SymmoeError`` on a
+non-zero return.  Every step of the path runs in the library's CUDA kernels;
+torch is used for device memory and streams only.  There is no CPU fallback:
+importing the package fails loudly if the library has not been built
+(``python -m combine_symmetric_heap_gb300.build``).
+
+``SymHeap`` is a convenience owner of one heap allocation (a torch uint8
+tensor) with zero-copy tensor views of its windows, e.g.
+``heap.combine_in_view()`` -- the expert-output window whose ``data_ptr``
+``moe_combine`` recognises (MORI CCO blog, "Zero-copy MoE dispatch -> expert
+-> combine": combine skips its staging copy when the expert wrote into the
+view it handed out).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libsymmoe.so")
+
+SYM_OK = 0
+SYM_EINVAL = -1
+SYM_ENOSPACE = -2
+SYM_ECUDA = -3
+SYM_ETIMEOUT = -4
+SYM_EOVERFLOW = -5
+SYM_ENOTSUP = -6
+SYM_STATUS_TIMEOUT = 0x1
+SYM_STATUS_OVERFLOW = 0x2
+SYM_ROWS_PER_FLAG = 128
+SYM_COUNT_CHUNK = 128
+
+_u64 = ctypes.c_uint64
+_u32 = ctypes.c_uint32
+_i32 = ctypes.c_int32
+_vp = ctypes.c_void_p
+
+
+class MoeShape(ctypes.Structure):
+    _fields_ = [("world", _i32), ("tokens_per_slot", _i32), ("hidden", _i32),
+                ("inter", _i32), ("num_experts", _i32), ("topk", _i32)]
+
+
+class SymHeapDesc(ctypes.Structure):
+    _fields_ = [("base", _u64), ("per_rank_size", _u64), ("bytes", _u64), ("cap", _u64),
+                ("off_recv_x", _u64), ("off_y", _u64), ("off_h", _u64),
+                ("off_recv_pair", _u64), ("off_recv_w", _u64), ("off_pos", _u64),
+                ("off_cnt", _u64), ("off_recv_off", _u64), ("off_total", _u64),
+                ("off_status", _u64), ("off_ready", _u64), ("off_hist", _u64),
+                ("off_ctrl", _u64), ("num_ready", _u32), ("epoch", _u32),
+                ("wait_timeout_us", _u32), ("reserved", _u32), ("s", MoeShape)]
+
+
+class SymmoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {sym_strerror(code)} ({code})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libsymmoe.so not built ({LIB_PATH}); run "
+                               "python -m combine_symmetric_heap_gb300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER
+        L.sym_heap_bytes.argtypes = [P(MoeShape), _u64, P(_u64), P(_u64)]
+        L.sym_heap_init.argtypes = [P(MoeShape), _vp, _u64, _u64, P(SymHeapDesc)]
+        L.sym_heap_slot_ptr.argtypes = [P(SymHeapDesc), ctypes.c_int, _u64]
+        L.sym_heap_slot_ptr.restype = _vp
+        L.moe_route_topk.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
+        L.moe_dispatch.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
+        L.moe_expert_ffn.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
+        L.moe_combine.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp, _vp]
+        L.moe_combine_fallback_copies.restype = _u64
+        L.moe_pipeline.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                   ctypes.c_int, _vp]
+        L.sym_heap_status.argtypes = [P(SymHeapDesc), P(_i32), ctypes.c_int, _vp]
+        L.sym_strerror.argtypes = [ctypes.c_int]
+        L.sym_strerror.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(s, torch.cuda.Stream):
+        return s.cuda_stream
+    return int(s)
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != SYM_OK:
+        raise SymmoeError(rc, where)
+
+
+def _shape(shape) -> MoeShape:
+    if isinstance(shape, MoeShape):
+        return shape
+    return MoeShape(shape["world"], shape["tokens_per_slot"], shape["hidden"], shape["inter"],
+                    shape["num_experts"], shape["topk"])
+
+
+# ------------------------------------------------------------------ C calls
+
+def sym_strerror(code: int) -> str:
+    return lib().sym_strerror(code).decode()
+
+
+def sym_heap_bytes(shape, align: int = 0):
+    prs, tot = _u64(), _u64()
+    s = _shape(shape)
+    _check(lib().sym_heap_bytes(ctypes.byref(s), align, ctypes.byref(prs), ctypes.byref(tot)),
+           "sym_heap_bytes")
+    return prs.value, tot.value
+
+
+def sym_heap_init(shape, dev_base, nbytes: int, align: int = 0) -> SymHeapDesc:
+    out = SymHeapDesc()
+    s = _shape(shape)
+    _check(lib().sym_heap_init(ctypes.byref(s), _ptr(dev_base), nbytes, align, ctypes.byref(out)),
+           "sym_heap_init")
+    return out
+
+
+def sym_heap_slot_ptr(heap: SymHeapDesc, slot: int, offset: int) -> int | None:
+    return lib().sym_heap_slot_ptr(ctypes.byref(heap), slot, offset)
+
+
+def moe_route_topk(heap: SymHeapDesc, logits, idx, w, stream=None) -> None:
+    _check(lib().moe_route_topk(ctypes.byref(heap), _ptr(logits), _ptr(idx), _ptr(w),
+                                _stream(stream)), "moe_route_topk")
+
+
+def moe_dispatch(heap: SymHeapDesc, x, idx, w, stream=None) -> None:
+    _check(lib().moe_dispatch(ctypes.byref(heap), _ptr(x), _ptr(idx), _ptr(w), _stream(stream)),
+           "moe_dispatch")
+
+
+def moe_expert_ffn(heap: SymHeapDesc, w_gate, w_up, w_down, stream=None) -> None:
+    _check(lib().moe_expert_ffn(ctypes.byref(heap), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                                _stream(stream)), "moe_expert_ffn")
+
+
+def moe_combine(heap: SymHeapDesc, expert_out, idx, w, out, stream=None) -> None:
+    _check(lib().moe_combine(ctypes.byref(heap), _ptr(expert_out), _ptr(idx), _ptr(w), _ptr(out),
+                             _stream(stream)), "moe_combine")
+
+
+def moe_combine_fallback_copies() -> int:
+    return int(lib().moe_combine_fallback_copies())
+
+
+def moe_pipeline(heap: SymHeapDesc, logits, x, w_gate, w_up, w_down, idx, w, out,
+                 fused: int = 0, stream=None) -> None:
+    _check(lib().moe_pipeline(ctypes.byref(heap), _ptr(logits), _ptr(x), _ptr(w_gate),
+                              _ptr(w_up), _ptr(w_down), _ptr(idx), _ptr(w), _ptr(out),
+                              int(fused), _stream(stream)), "moe_pipeline")
+
+
+def sym_heap_status(heap: SymHeapDesc, clear: bool = False, stream=None) -> int:
+    st = _i32()
+    _check(lib().sym_heap_status(ctypes.byref(heap), ctypes.byref(st), int(clear), _stream(stream)),
+           "sym_heap_status")
+    return st.value
+
+
+# ------------------------------------------------------------------ heap owner
+
+class SymHeap:
+    """One symmetric heap in a torch-owned device allocation, with views.
+
+    Every view is a slice of ``self.buf`` (no copy); slot ``d``'s copy of a
+    window starts at ``d * per_rank_size + off``.
+    """
+
+    def __init__(self, shape: dict, device="cuda", align: int = 0):
+        self.shape = dict(shape)
+        prs, total = sym_heap_bytes(shape, align)
+        self.buf = torch.empty(total + 256, dtype=torch.uint8, device=device)
+        pad = (-self.buf.data_ptr()) % 256
+        self.buf = self.buf[pad:pad + total]
+        self.desc = sym_heap_init(shape, self.buf.data_ptr(), total, align)
+
+    # raw window views --------------------------------------------------
+    def _win(self, slot: int, off: int, nbytes: int, dtype) -> torch.Tensor:
+        base = slot * self.desc.per_rank_size + off
+        return self.buf[base:base + nbytes].view(dtype)
+
+    @property
+    def cap(self) -> int:
+        return self.desc.cap
+
+    def recv_x(self, d: int) -> torch.Tensor:
+        H = self.shape["hidden"]
+        return self._win(d, self.desc.off_recv_x, self.cap * H * 2, torch.bfloat16).view(self.cap, H)
+
+    def y(self, d: int) -> torch.Tensor:
+        H = self.shape["hidden"]
+        return self._win(d, self.desc.off_y, self.cap * H * 2, torch.bfloat16).view(self.cap, H)
+
+    def h(self, d: int) -> torch.Tensor:
+        I = self.shape["inter"]
+        return self._win(d, self.desc.off_h, self.cap * I * 2, torch.bfloat16).view(self.cap, I)
+
+    def recv_pair(self, d: int) -> torch.Tensor:
+        return self._win(d, self.desc.off_recv_pair, self.cap * 4, torch.int32)
+
+    def recv_w(self, d: int) -> torch.Tensor:
+        return self._win(d, self.desc.off_recv_w, self.cap * 4, torch.float32)
+
+    def pos(self, d: int) -> torch.Tensor:
+        T, k = self.shape["tokens_per_slot"], self.shape["topk"]
+        return self._win(d, self.desc.off_pos, T * k * 4, torch.int32).view(T, k)
+
+    def cnt(self, d: int) -> torch.Tensor:
+        el = self.shape["num_experts"] // self.shape["world"]
+        return self._win(d, self.desc.off_cnt, el * 4, torch.int32)
+
+    def recv_off(self, d: int) -> torch.Tensor:
+        el = self.shape["num_experts"] // self.shape["world"]
+        return self._win(d, self.desc.off_recv_off, el * 4, torch.int32)
+
+    def total_recv(self, d: int) -> torch.Tensor:
+        return self._win(d, self.desc.off_total, 4, torch.int32)
+
+    def ready(self, d: int) -> torch.Tensor:
+        return self._win(d, self.desc.off_ready, self.desc.num_ready * 4, torch.int32)
+
+    def combine_in_view(self) -> torch.Tensor:
+        """Expert-output window as [W, cap, H] (strided by the slot size);
+        its data_ptr is the one moe_combine treats as zero-copy."""
+        H = self.shape["hidden"]
+        W = self.shape["world"]
+        base = self.buf[self.desc.off_y:].view(torch.bfloat16)
+        return base.as_strided((W, self.cap, H), (self.desc.per_rank_size // 2, H, 1))
+
+    def status(self, clear: bool = False, stream=None) -> int:
+        return sym_heap_status(self.desc, clear, stream)
+
+    # calls -----------------------------------------------------------------
+    def route_topk(self, logits, idx, w, stream=None):
+        moe_route_topk(self.desc, logits, idx, w, stream)
+
+    def dispatch(self, x, idx, w, stream=None):
+        moe_dispatch(self.desc, x, idx, w, stream)
+
+    def expert_ffn(self, wg, wu, wd, stream=None):
+        moe_expert_ffn(self.desc, wg, wu, wd, stream)
+
+    def combine(self, idx, w, out, expert_out=None, stream=None):
+        moe_combine(self.desc, expert_out, idx, w, out, stream)
+
+    def pipeline(self, logits, x, wg, wu, wd, idx, w, out, fused=0, stream=None):
+        moe_pipeline(self.desc, logits, x, wg, wu, wd, idx, w, out, fused, stream)
+
+
+lib()  # fail loudly at import if the CUDA library is missing

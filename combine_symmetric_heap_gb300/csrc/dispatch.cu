@@ -1,0 +1,201 @@
+// dispatch.cu -- the all-to-all scatter of the zero-copy MoE pipeline.
+//
+// MORI CCO blog, "Zero-copy MoE dispatch -> expert -> combine": each rank
+// writes its tokens directly into the receive window ("disp_out") of the rank
+// that owns each selected expert, with no staging copy.  Here every rank is a
+// slot of one heap and the "peer store" is a 16-byte vector store to
+// base + slot * per_rank_size + off_recv_x + row * H * 2.
+//
+// Receive order (the pages leave it open): rows grouped by expert, experts
+// ascending inside a slot; inside one expert by (source slot, token, k),
+// i.e. by global token g because the k experts of a token are distinct.
+//
+// Three launches:
+//   count   one CTA per 128-token chunk: per-expert bitmask of the chunk's
+//           tokens in shared memory -> each pair's rank inside the chunk
+//           (popcount of the lower bits) and the chunk histogram.
+//   scan    one CTA: exclusive scan of the chunk histograms per expert (warp
+//           scans), expert counts, receive offsets per slot, total rows per
+//           slot; clears the ready counters for this call.
+//   scatter one CTA per token: x[g] is read once and stored k times (one per
+//           destination), then recv_pair / recv_w / pos are written and the
+//           ready counter of each destination row block is raised.
+#include "symmoe_dev.cuh"
+
+namespace symmoe {
+
+constexpr int CHUNK = SYM_COUNT_CHUNK;  // 128 tokens: 4 mask words per expert
+
+__global__ void __launch_bounds__(CHUNK) dispatch_count_kernel(sym_heap h,
+                                                               const int32_t *__restrict__ idx) {
+  extern __shared__ uint32_t mask[];  // [E][CHUNK/32]
+  const int E = h.s.num_experts, k = h.s.topk, T = h.s.tokens_per_slot;
+  const int N = h.s.world * T;
+  const int nchunks = (N + CHUNK - 1) / CHUNK;
+  const int chunk = blockIdx.x;
+  const int t = threadIdx.x;
+  const int g = chunk * CHUNK + t;
+  for (int i = t; i < E * (CHUNK / 32); i += CHUNK) mask[i] = 0;
+  __syncthreads();
+  const uint32_t bit = 1u << (t & 31);
+  const int word = t >> 5;
+  if (g < N) {
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[(size_t)g * k + j];
+      if (e < 0 || e >= E) {
+        raise_status(h, SYM_STATUS_OVERFLOW);
+        continue;
+      }
+      const uint32_t old = atomicOr(&mask[e * (CHUNK / 32) + word], bit);
+      if (old & bit) raise_status(h, SYM_STATUS_OVERFLOW);  // duplicate expert in a token
+    }
+  }
+  __syncthreads();
+  if (g < N) {
+    int32_t *pos = win<int32_t>(h, g / T, h.off_pos) + (size_t)(g % T) * k;
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[(size_t)g * k + j];
+      int r = -1;
+      if (e >= 0 && e < E) {
+        const uint32_t *m = mask + e * (CHUNK / 32);
+        r = __popc(m[word] & (bit - 1u));
+        for (int w = 0; w < word; ++w) r += __popc(m[w]);
+      }
+      pos[j] = r;  // rank inside the chunk; the scatter adds the bases
+    }
+  }
+  int32_t *hist = win<int32_t>(h, 0, h.off_hist);  // [E][nchunks]
+  for (int e = t; e < E; e += CHUNK) {
+    const uint32_t *m = mask + e * (CHUNK / 32);
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < CHUNK / 32; ++w) c += __popc(m[w]);
+    hist[(size_t)e * nchunks + chunk] = c;
+  }
+}
+
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(sym_heap h) {
+  __shared__ int32_t cnt_s[1024];
+  const int E = h.s.num_experts, W = h.s.world;
+  const int E_loc = E / W;
+  const int N = W * h.s.tokens_per_slot;
+  const int nchunks = (N + CHUNK - 1) / CHUNK;
+  int32_t *hist = win<int32_t>(h, 0, h.off_hist);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  // per expert: exclusive scan over chunks (warp scan, 32 chunks at a time)
+  for (int e = wid; e < E; e += nw) {
+    int32_t *row = hist + (size_t)e * nchunks;
+    int carry = 0;
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c < nchunks ? row[c] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (c < nchunks) row[c] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) cnt_s[e] = carry;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int d = e / E_loc, l = e % E_loc;
+    int off = 0;
+    for (int i = 0; i < l; ++i) off += cnt_s[d * E_loc + i];
+    win<int32_t>(h, d, h.off_cnt)[l] = cnt_s[e];
+    win<int32_t>(h, d, h.off_recv_off)[l] = off;
+    if (l == E_loc - 1) *win<int32_t>(h, d, h.off_total) = off + cnt_s[e];
+  }
+  for (int i = threadIdx.x; i < W * (int)h.num_ready; i += blockDim.x)
+    win<uint32_t>(h, i / h.num_ready, h.off_ready)[i % h.num_ready] = 0u;
+}
+
+constexpr int SCATTER_THREADS = 128;
+constexpr int SCATTER_VEC_PER_THREAD = 8;  // H <= 128*8*8 = 8192 in one pass
+
+__global__ void __launch_bounds__(SCATTER_THREADS)
+    dispatch_scatter_kernel(sym_heap h, const uint4 *__restrict__ x,
+                            const int32_t *__restrict__ idx, const float *__restrict__ w) {
+  __shared__ uint4 *dst_s[32];
+  __shared__ int32_t slot_s[32], row_s[32];
+  const int E = h.s.num_experts, k = h.s.topk, T = h.s.tokens_per_slot, H = h.s.hidden;
+  const int E_loc = E / h.s.world;
+  const int N = h.s.world * T;
+  const int nchunks = (N + CHUNK - 1) / CHUNK;
+  const int g = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nvec = H / 8;  // 16-byte vectors per row
+  const uint4 *src = x + (size_t)g * nvec;
+
+  // start the row loads before resolving the destinations
+  uint4 v[SCATTER_VEC_PER_THREAD];
+#pragma unroll
+  for (int i = 0; i < SCATTER_VEC_PER_THREAD; ++i) {
+    const int c = tid + i * SCATTER_THREADS;
+    if (c < nvec) v[i] = __ldg(src + c);
+  }
+  if (tid < k) {
+    const int j = tid;
+    const int e = idx[(size_t)g * k + j];
+    int32_t *pos = win<int32_t>(h, g / T, h.off_pos) + (size_t)(g % T) * k;
+    uint4 *dst = nullptr;
+    int d = -1, p = -1;
+    if (e >= 0 && e < E) {
+      d = e / E_loc;
+      const int l = e % E_loc;
+      const int rank = pos[j];
+      p = win<int32_t>(h, d, h.off_recv_off)[l] +
+          win<int32_t>(h, 0, h.off_hist)[(size_t)e * nchunks + g / CHUNK] + rank;
+      if (rank < 0 || p < 0 || (uint64_t)p >= h.cap) {
+        raise_status(h, SYM_STATUS_OVERFLOW);
+        p = -1;
+      } else {
+        dst = win<uint4>(h, d, h.off_recv_x) + (size_t)p * nvec;
+      }
+    }
+    pos[j] = p;
+    dst_s[j] = dst;
+    slot_s[j] = d;
+    row_s[j] = p;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < SCATTER_VEC_PER_THREAD; ++i) {
+    const int c = tid + i * SCATTER_THREADS;
+    if (c < nvec)
+      for (int j = 0; j < k; ++j)
+        if (dst_s[j]) dst_s[j][c] = v[i];
+  }
+  // rows wider than one pass
+  for (int c = tid + SCATTER_VEC_PER_THREAD * SCATTER_THREADS; c < nvec; c += SCATTER_THREADS) {
+    const uint4 u = __ldg(src + c);
+    for (int j = 0; j < k; ++j)
+      if (dst_s[j]) dst_s[j][c] = u;
+  }
+  if (tid < k && row_s[tid] >= 0) {
+    const int d = slot_s[tid], p = row_s[tid];
+    win<int32_t>(h, d, h.off_recv_pair)[p] = g * k + tid;
+    win<float>(h, d, h.off_recv_w)[p] = w[(size_t)g * k + tid];
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid < k && row_s[tid] >= 0)
+    atomicAdd(win<uint32_t>(h, slot_s[tid], h.off_ready) + row_s[tid] / SYM_ROWS_PER_FLAG, 1u);
+}
+
+cudaError_t launch_dispatch(const sym_heap &h, const uint16_t *x, const int32_t *idx,
+                            const float *w, cudaStream_t st) {
+  const int N = h.s.world * h.s.tokens_per_slot;
+  const int nchunks = (N + CHUNK - 1) / CHUNK;
+  const size_t mask_bytes = (size_t)h.s.num_experts * (CHUNK / 32) * sizeof(uint32_t);
+  dispatch_count_kernel<<<nchunks, CHUNK, mask_bytes, st>>>(h, idx);
+  dispatch_scan_kernel<<<1, 1024, 0, st>>>(h);
+  dispatch_scatter_kernel<<<N, SCATTER_THREADS, 0, st>>>(h, reinterpret_cast<const uint4 *>(x),
+                                                          idx, w);
+  return cudaGetLastError();
+}
+
+}  // namespace symmoe

@@ -1,0 +1,229 @@
+/*
+ * symmoe.h -- C ABI of the zero-copy MoE dispatch -> expert -> combine path
+ * over a flat symmetric heap, for one GB300 (sm_103a).
+ *
+ * Source of the operations: the AMD technical blog "MORI CCO: Next-Generation
+ * Collective Communication Object for GPUs" --
+ *   - section "What is MORI CCO?": every window sits at the same offset in
+ *     every rank's slot, so a peer address is window base + peer * per-rank
+ *     size + offset;
+ *   - section "Zero-copy MoE dispatch -> expert -> combine": dispatch writes
+ *     each token straight into the receive window ("disp_out") of the rank
+ *     that owns its expert, the expert GEMM reads that window in place and
+ *     writes its output into the combine staging window ("out_tok", the
+ *     combine_in view), and combine gathers those rows back, weighted;
+ *   - section "Mega-MoE: mega-kernel co-design with FlyDSL": dispatch, expert
+ *     GEMM and combine fused into one kernel launch;
+ * and the "MORI CCO Guide", sections "1. Concepts" (device communicator
+ * passed by value into kernels) and "3. Memory and Windows" (collective
+ * registration at identical offsets).
+ *
+ * Here the W "ranks" are W logical slots carved at identical offsets inside
+ * ONE device allocation; a cross-slot store is a plain global store to
+ * base + slot * per_rank_size + offset.
+ *
+ * Conventions for every call:
+ *   - All pointers named dev_* or documented as device pointers must point to
+ *     device memory of the current CUDA device; the library never allocates,
+ *     frees or copies to/from host memory except in sym_heap_status (which
+ *     reads one status word) -- the caller owns every buffer.
+ *   - bf16 tensors are passed as uint16_t bit patterns, row-major, contiguous.
+ *   - All compute calls are asynchronous on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and never synchronise the host.
+ *   - Return value: SYM_OK (0) or a negative SYM_E* code, detected
+ *     synchronously (bad argument, too small a heap, launch failure).
+ *     Conditions found on the device while a kernel runs (a bounded wait that
+ *     expired, a row beyond capacity) are OR-ed into the heap's status word
+ *     and read with sym_heap_status; no kernel traps or aborts.
+ *
+ * Shapes (moe_shape): W = world slots, T = tokens per slot, N = W*T global
+ * tokens (global token g = s*T + t lives on slot s), H = hidden, I = expert
+ * intermediate size, E = experts, E/W experts per slot (expert e lives on
+ * slot e / (E/W)), k = top-k.  Limits: E % W == 0, 1 <= k <= min(E, 32),
+ * E <= 1024, H % 128 == 0, I % 128 == 0, H, I <= 65536.
+ */
+#ifndef SYMMOE_H
+#define SYMMOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *symmoe_stream_t; /* == cudaStream_t */
+
+/* ---- status codes -------------------------------------------------------- */
+#define SYM_OK 0
+#define SYM_EINVAL (-1)    /* bad shape, pointer, alignment or argument        */
+#define SYM_ENOSPACE (-2)  /* heap smaller than sym_heap_bytes() requires      */
+#define SYM_ECUDA (-3)     /* a CUDA runtime call or kernel launch failed      */
+#define SYM_ETIMEOUT (-4)  /* (status word) a bounded device wait expired      */
+#define SYM_EOVERFLOW (-5) /* (status word) a row index beyond its window      */
+#define SYM_ENOTSUP (-6)   /* not supported on this device (needs sm_103a)     */
+
+/* bits of the device status word */
+#define SYM_STATUS_TIMEOUT 0x1
+#define SYM_STATUS_OVERFLOW 0x2
+
+/* rows covered by one dispatch ready counter (per slot, per row block) */
+#define SYM_ROWS_PER_FLAG 128
+/* tokens per dispatch counting chunk */
+#define SYM_COUNT_CHUNK 128
+
+typedef struct moe_shape {
+  int32_t world;           /* W */
+  int32_t tokens_per_slot; /* T */
+  int32_t hidden;          /* H */
+  int32_t inter;           /* I */
+  int32_t num_experts;     /* E */
+  int32_t topk;            /* k */
+} moe_shape;
+
+/*
+ * sym_heap: the symmetric heap descriptor.  Plain old data, passed BY VALUE
+ * into every kernel (the device-communicator rule of the CCO guide).  Every
+ * off_* is a byte offset inside EACH slot; window w of slot d is at
+ * base + d * per_rank_size + off_w.  Per-slot windows:
+ *   recv_x    [cap][H] bf16  dispatched token rows ("disp_out")
+ *   y         [cap][H] bf16  expert outputs ("out_tok", combine_in view)
+ *   h         [cap][I] bf16  SwiGLU intermediate of the expert FFN
+ *   recv_pair [cap] int32    g*k + j of the pair that filled each row
+ *   recv_w    [cap] fp32     routing weight of that pair
+ *   pos       [T][k] int32   receive row of each of this slot's own pairs
+ *                            (the "routing" handle combine uses)
+ *   signal area: cnt [E/W] int32, recv_off [E/W] int32, total_recv int32,
+ *                status int32 (slot 0's is the heap status word),
+ *                ready [ceil(cap/128)] uint32 (rows landed per 128-row block)
+ *   scratch (used in slot 0 only): dispatch chunk histograms, fused-kernel
+ *                control block.
+ * Receive rows are grouped by expert (ascending) inside a slot; inside one
+ * expert they are in (source slot, token, k) order.
+ */
+typedef struct sym_heap {
+  uint64_t base;          /* device address of slot 0                          */
+  uint64_t per_rank_size; /* slot stride in bytes (multiple of align)          */
+  uint64_t bytes;         /* W * per_rank_size                                 */
+  uint64_t cap;           /* receive rows per slot = N * min(k, E/W)           */
+  uint64_t off_recv_x, off_y, off_h, off_recv_pair, off_recv_w, off_pos;
+  uint64_t off_cnt, off_recv_off, off_total, off_status, off_ready;
+  uint64_t off_hist;      /* [ceil(N/128)][E] int32                            */
+  uint64_t off_ctrl;      /* fused-kernel control block (256 bytes)            */
+  uint32_t num_ready;     /* ready counters per slot = ceil(cap / 128)         */
+  uint32_t epoch;         /* bumped by every dispatch / pipeline call          */
+  uint32_t wait_timeout_us; /* bound on every device-side wait (default 2 s)   */
+  uint32_t reserved;
+  moe_shape s;
+} sym_heap;
+
+/*
+ * sym_heap_bytes: size of the heap a shape needs.
+ *   align: slot stride granularity in bytes (power of two >= 256; 0 = 2 MiB).
+ *          align = 1<<32 reproduces the CCO kernel's 4 GiB-multiple stride.
+ *   per_rank_size (out, may be NULL), total_bytes (out, may be NULL).
+ * Host only.  Returns SYM_OK or SYM_EINVAL.
+ */
+int sym_heap_bytes(const moe_shape *s, uint64_t align, uint64_t *per_rank_size,
+                   uint64_t *total_bytes);
+
+/*
+ * sym_heap_init: carve the windows into a caller-owned device allocation
+ * (collective "alloc + register" of the CCO guide, reduced to arithmetic:
+ * same windows, same order, same offsets in every slot).
+ *   dev_base: device pointer, 256-byte aligned, owned by the caller, at least
+ *             sym_heap_bytes(...) bytes; the library keeps no reference other
+ *             than the copy in *out.
+ *   out:      filled descriptor (epoch 0, wait_timeout_us 2,000,000).
+ * Host only, no device access.  SYM_EINVAL on a bad shape or alignment,
+ * SYM_ENOSPACE if bytes is too small.
+ */
+int sym_heap_init(const moe_shape *s, void *dev_base, uint64_t bytes, uint64_t align,
+                  sym_heap *out);
+
+/*
+ * sym_heap_slot_ptr: base + slot * per_rank_size + offset (the peer address
+ * of "What is MORI CCO?").  Returns NULL if slot or offset is out of range.
+ */
+void *sym_heap_slot_ptr(const sym_heap *h, int slot, uint64_t offset);
+
+/*
+ * moe_route_topk: per token, the top-k of E fp32 logits (descending, ties to
+ * the lower expert index) and softmax weights over the selected k.
+ *   logits: device [N][E] fp32;  idx: device [N][k] int32 (out);
+ *   w: device [N][k] fp32 (out).  The pages leave routing to the caller; this
+ *   is the router that feeds moe_dispatch.
+ */
+int moe_route_topk(const sym_heap *h, const float *logits, int32_t *idx, float *w,
+                   symmoe_stream_t stream);
+
+/*
+ * moe_dispatch: the all-to-all scatter of "Zero-copy MoE dispatch".
+ * Counts pairs per expert, builds receive offsets, and copies every token row
+ * x[g] into slot (idx[g][j] / (E/W))'s recv_x window at its receive row
+ * (16-byte vector stores), writing recv_pair / recv_w / pos and raising the
+ * ready counters (release) of the row blocks it fills.
+ *   x: device [N][H] bf16;  idx, w: device [N][k] (from moe_route_topk or the
+ *   caller; every idx must be in [0, E) and the k experts of a token distinct).
+ *   Bumps h->epoch.  Out-of-range rows are skipped and flagged
+ *   SYM_STATUS_OVERFLOW in the status word.
+ */
+int moe_dispatch(sym_heap *h, const uint16_t *x, const int32_t *idx, const float *w,
+                 symmoe_stream_t stream);
+
+/*
+ * moe_expert_ffn: expert_gemm of "Zero-copy MoE dispatch", here a SwiGLU FFN
+ * per expert on its received rows, in place on the heap:
+ *   h = bf16(silu(recv_x Wg_e^T) * (recv_x Wu_e^T)),  y = bf16(h Wd_e^T),
+ * fp32 accumulation on the tensor cores (tcgen05, TMEM, TMA).  Row counts are
+ * read on the device (no host sync); before loading a row block the kernel
+ * waits (bounded) for its dispatch ready counter.
+ *   w_gate, w_up: device [E][I][H] bf16;  w_down: device [E][H][I] bf16.
+ * Writes the h and y windows of every slot.
+ */
+int moe_expert_ffn(const sym_heap *h, const uint16_t *w_gate, const uint16_t *w_up,
+                   const uint16_t *w_down, symmoe_stream_t stream);
+
+/*
+ * moe_combine: the weighted all-to-all gather of "Zero-copy MoE dispatch":
+ *   out[g] = bf16( sum_{j<k} w[g][j] * y[slot(idx[g][j])][pos[g][j]] ),
+ * fp32 accumulation in j order.
+ *   expert_out: NULL or the address of slot 0's y window -> zero copy (the
+ *     data_ptr match of the pages).  Any other device pointer is read as a
+ *     dense [W][cap][H] bf16 tensor whose rows [0, total_recv[d]) are first
+ *     copied into the y windows (the pages' silent fallback copy; counted by
+ *     moe_combine_fallback_copies), with the identical result.
+ *   idx, w: device [N][k] as given to moe_dispatch;  out: device [N][H] bf16.
+ */
+int moe_combine(const sym_heap *h, const uint16_t *expert_out, const int32_t *idx,
+                const float *w, uint16_t *out, symmoe_stream_t stream);
+
+/* Number of fallback copies moe_combine has made in this process. */
+uint64_t moe_combine_fallback_copies(void);
+
+/*
+ * moe_pipeline: route -> dispatch -> expert FFN -> combine on one stream.
+ *   fused = 0: one launch per stage (7 kernels).
+ *   fused = 1: one persistent launch ("Mega-MoE"): expert tiles start as soon
+ *              as the ready counters of their rows land.
+ *   idx, w: device [N][k] outputs of the routing step; out: device [N][H].
+ *   Bumps h->epoch.
+ */
+int moe_pipeline(sym_heap *h, const float *logits, const uint16_t *x, const uint16_t *w_gate,
+                 const uint16_t *w_up, const uint16_t *w_down, int32_t *idx, float *w,
+                 uint16_t *out, int fused, symmoe_stream_t stream);
+
+/*
+ * sym_heap_status: synchronises `stream`, reads the heap status word (slot 0)
+ * into *status (SYM_STATUS_* bits) and, if clear != 0, resets it to 0.
+ * Returns SYM_OK, SYM_EINVAL or SYM_ECUDA.
+ */
+int sym_heap_status(const sym_heap *h, int32_t *status, int clear, symmoe_stream_t stream);
+
+/* Static description of a SYM_* code (never NULL). */
+const char *sym_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SYMMOE_H */

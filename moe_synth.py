@@ -271,6 +271,17 @@ def x_torch(cfg: dict, device, seed: int = 0):
     return fill_normal_bf16_torch(out, seed, STREAM_X, 0, X_SIGMA)
 
 
+def weight_expert_torch(cfg: dict, which: str, expert: int, device, seed: int = 0):
+    """One expert's weight, generated afresh by the torch implementation:
+    'gate'/'up' [I,H], 'down' [H,I] bf16 (the same bits as ``weight_np``)."""
+    import torch
+    h, i = cfg["hidden"], cfg["inter"]
+    stream = {"gate": STREAM_WG, "up": STREAM_WU, "down": STREAM_WD}[which]
+    rows, cols = (i, h) if which in ("gate", "up") else (h, i)
+    out = torch.empty((rows, cols), dtype=torch.bfloat16, device=device)
+    return fill_normal_bf16_torch(out, seed, stream, expert * rows * cols, W_SIGMA)
+
+
 def weights_torch(cfg: dict, device, seed: int = 0):
     """(W_gate [E,I,H], W_up [E,I,H], W_down [E,H,I]) bf16 on ``device``."""
     import torch
