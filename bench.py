@@ -1,0 +1,416 @@
+"""Benchmark: MoE route -> dispatch -> expert -> combine tokens/s on GB300.
+
+One step = one pass of the whole path (route, dispatch, SwiGLU expert FFN,
+combine) over one batch of N = W*T synthetic tokens.  Default workload:
+Mixtral-like (W=8 slots, T=2048, H=4096, E=8, k=2, I=14336).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--fused]
+    python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Prints one JSON line.  With N > 1 (torchrun, one rank per GPU) every rank runs
+an independent replica of the workload (the path has no inter-GPU exchange on
+one box) and the value is the tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE dispatch+expert+combine tokens/s on 1 GB300; % HBM / bf16 tensor roofline"
+UNIT = "tokens/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--config", default="mixtral")
+    p.add_argument("--fused", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_config(name: str, cfg: dict, fused: bool) -> dict:
+    import moe_synth as ms
+    n = cfg["world"] * cfg["tokens_per_slot"]
+    return {"workload": ms.CONFIG_TITLES.get(name, name), "preset": name,
+            "world_slots": cfg["world"], "tokens_per_slot": cfg["tokens_per_slot"],
+            "tokens_per_step": n, "hidden": cfg["hidden"], "inter": cfg["inter"],
+            "experts": cfg["num_experts"], "topk": cfg["topk"], "fused": bool(fused),
+            "l2": "inputs larger than L2 (expert weights alone exceed 129 MB)",
+            "parallelism": "replicas"}
+
+
+def algorithmic(cfg: dict) -> dict:
+    n = cfg["world"] * cfg["tokens_per_slot"]
+    k, H, I, E = cfg["topk"], cfg["hidden"], cfg["inter"], cfg["num_experts"]
+    P = n * k
+    return {
+        "route_bytes": n * E * 4 + n * k * 8,
+        "dispatch_bytes": n * H * 2 * (1 + k),
+        "ffn_flops": 6 * P * H * I,
+        "combine_bytes": P * H * 2 + n * H * 2,
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_record(kernel_file: str):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, or None if the kernel source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path))
+        src = open(os.path.join(ROOT, "combine_symmetric_heap_gb300", "csrc", kernel_file), "rb").read()
+        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        return rec.get("traffic_bytes_per_step")
+    except Exception:
+        return None
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_run(cfg: dict, tokens, weights: dict):
+    """Time the oracle, as it stands, over a sample of tokens: routing of the
+    sample, placement of its pairs, the SwiGLU FFN of every received row, and
+    the combine.  ``weights[e]`` are the experts' bf16 bits (inputs, not timed
+    as oracle work).  Returns seconds."""
+    import numpy as np
+    import moe_synth as ms
+    import oracle
+    lg = ms.logits_np(cfg, rows=tokens)
+    xs = ms.x_np(cfg, rows=tokens)
+    t0 = time.perf_counter()
+    sample = dict(cfg, tokens_per_slot=len(tokens), world=1, num_experts=cfg["num_experts"])
+    res = oracle.pipeline(lg, xs, dict(world=1, num_experts=cfg["num_experts"], topk=cfg["topk"]),
+                          lambda e: weights[e])
+    dt = time.perf_counter() - t0
+    assert res["out"].shape == (len(tokens), cfg["hidden"])
+    del sample
+    return dt
+
+
+def sample_weights(cfg: dict, tokens, device):
+    """Fresh host copies of the experts the sample tokens route to."""
+    import numpy as np
+    import moe_synth as ms
+    import oracle
+    idx, _ = oracle.route_topk(ms.logits_np(cfg, rows=tokens), cfg["topk"])
+    out = {}
+    for e in sorted(set(idx.reshape(-1).tolist())):
+        if device is not None:
+            out[e] = tuple(ms.weight_expert_torch(cfg, nm, e, device).view(__import__("torch").int16)
+                           .cpu().numpy().view(np.uint16) for nm in ("gate", "up", "down"))
+        else:
+            out[e] = tuple(ms.weight_np(cfg, nm, e) for nm in ("gate", "up", "down"))
+    return out
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+    import moe_synth as ms
+    cfg = ms.CONFIGS[args.config]
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else None
+    per_step = int(os.environ.get("SYMMOE_REF_TOKENS", "8"))
+    n = cfg["world"] * cfg["tokens_per_slot"]
+    rng = np.random.default_rng(0)
+    times = []
+    for s in range(args.warmup + args.steps):
+        tokens = np.sort(rng.choice(n, size=per_step, replace=False))
+        wts = sample_weights(cfg, tokens, dev)
+        dt = oracle_sample_run(cfg, tokens, wts)
+        if s >= args.warmup:
+            times.append(dt)
+    tot = sum(times)
+    value = per_step * len(times) / tot
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(args.config, cfg, args.fused),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                         "sample": f"{per_step} random tokens of the workload per step (their "
+                                   f"routing, placement, expert FFN rows and combine); expert "
+                                   f"weights generated outside the timed region"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import moe_synth as ms
+    import combine_symmetric_heap_gb300 as sm
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = ms.CONFIGS[args.config]
+    fused = 1 if args.fused else 0
+    n, k, H = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"], cfg["hidden"]
+
+    heap = sm.SymHeap(cfg, dev)
+    logits = ms.logits_torch(cfg, dev)
+    x = ms.x_torch(cfg, dev)
+    wg, wu, wd = ms.weights_torch(cfg, dev)
+    idx = torch.empty((n, k), dtype=torch.int32, device=dev)
+    w = torch.empty((n, k), dtype=torch.float32, device=dev)
+    out = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def step():
+        heap.pipeline(logits, x, wg, wu, wd, idx, w, out, fused=fused, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert heap.status(stream=stream) == 0, "device status word set during warm-up"
+
+    # ---- timed region: K whole-path steps, device resident inputs
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    assert heap.status(stream=stream) == 0, "device status word set during the timed steps"
+    ms_step = ms_total / args.steps
+    value = n * args.steps * world / (ms_total / 1e3)
+    launches_per_step = 1 if fused else 7
+
+    # ---- stage times on the same stream (unfused calls, same kernels)
+    stages = {}
+    if not fused:
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        reps = max(3, min(args.steps, 20))
+        acc = [0.0] * 4
+        for _ in range(reps):
+            evs[0].record(stream)
+            heap.route_topk(logits, idx, w, stream=stream)
+            evs[1].record(stream)
+            heap.dispatch(x, idx, w, stream=stream)
+            evs[2].record(stream)
+            heap.expert_ffn(wg, wu, wd, stream=stream)
+            evs[3].record(stream)
+            heap.combine(idx, w, out, stream=stream)
+            evs[4].record(stream)
+            torch.cuda.synchronize()
+            for i in range(4):
+                acc[i] += evs[i].elapsed_time(evs[i + 1])
+        stages = dict(zip(["route", "dispatch", "expert_ffn", "combine"], [a / reps for a in acc]))
+
+    alg = algorithmic(cfg)
+    hbm, tf_burst, tf_sus, peak_src = peaks()
+    long_region = ms_total > 1000.0
+    tf_peak = tf_sus if long_region else tf_burst
+    roofline = None
+    if stages:
+        ffn_s = stages["expert_ffn"] / 1e3
+        achieved = alg["ffn_flops"] / ffn_s / 1e12
+        roofline = {"bound": "tensor", "kernel": "expert_gemm (SwiGLU gate/up + down launches)",
+                    "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
+                    "frac": achieved / tf_peak, "traffic": traffic_record("expert_ffn.cu"),
+                    "peak_kind": f"{peak_src} bf16 {'sustained' if long_region else 'burst'}",
+                    "algorithmic_flops_per_step": alg["ffn_flops"]}
+        stage_bw = {
+            "dispatch_gbs": alg["dispatch_bytes"] / (stages["dispatch"] / 1e3) / 1e9,
+            "combine_gbs": alg["combine_bytes"] / (stages["combine"] / 1e3) / 1e9,
+            "route_gbs": alg["route_bytes"] / (stages["route"] / 1e3) / 1e9,
+            "hbm_peak_gbs": hbm,
+        }
+        stage_bw["dispatch_frac"] = stage_bw["dispatch_gbs"] / hbm
+        stage_bw["combine_frac"] = stage_bw["combine_gbs"] / hbm
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        lg_h = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
+        x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        lg_h.copy_(logits)
+        x_h.copy_(x)
+        lg_d, x_d = torch.empty_like(logits), torch.empty_like(x)
+        e_steps = max(3, min(args.steps, 30))
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                lg_d.copy_(lg_h, non_blocking=True)
+                x_d.copy_(x_h, non_blocking=True)
+                heap.pipeline(lg_d, x_d, wg, wu, wd, idx, w, out, fused=fused, stream=stream)
+                out_h.copy_(out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": n * e_steps * world / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": lg_h.numel() * 4 + x_h.numel() * 2,
+               "d2h_bytes_per_step": out_h.numel() * 2, "steps": e_steps}
+
+    # ---- oracle on the host cores (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import numpy as np
+        ntok = int(os.environ.get("SYMMOE_CPU_TOKENS", "64"))
+        tokens = np.sort(np.random.default_rng(0).choice(n, size=ntok, replace=False))
+        wts = sample_weights(cfg, tokens, dev)
+        dt = oracle_sample_run(cfg, tokens, wts)
+        cpu = {"value": ntok / dt, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+               "sample": f"{ntok} random tokens of the workload (routing, placement, all "
+                         f"{ntok * k} expert FFN rows, combine) in {dt:.1f} s; fp64 numpy"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(args.config, cfg, fused),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+            "stages_ms": stages or None,
+            "stage_bandwidth": stage_bw if stages else None,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

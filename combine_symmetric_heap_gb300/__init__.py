@@ -6,7 +6,7 @@ arguments: torch tensors or raw device addresses in, ``SymmoeError`` on a
 non-zero return.  Every step of the path runs in the library's CUDA kernels;
 torch is used for device memory and streams only.  There is no CPU fallback:
 importing the package fails loudly if the library has not been built
-(``python -m combine_symmetric_heap_gb300.build``).
+(``python combine_symmetric_heap_gb300/build.py``).
 
 ``SymHeap`` is a convenience owner of one heap allocation (a torch uint8
 tensor) with zero-copy tensor views of its windows, e.g.
@@ -73,7 +73,7 @@ def lib() -> ctypes.CDLL:
     if _lib is None:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"libsymmoe.so not built ({LIB_PATH}); run "
-                               "python -m combine_symmetric_heap_gb300.build")
+                               "python combine_symmetric_heap_gb300/build.py")
         L = ctypes.CDLL(LIB_PATH)
         P = ctypes.POINTER
         L.sym_heap_bytes.argtypes = [P(MoeShape), _u64, P(_u64), P(_u64)]

@@ -1,6 +1,8 @@
 """Build libsymmoe.so (the C-ABI library) from csrc/*.cu with nvcc for sm_103a.
 
-Usage: ``python -m combine_symmetric_heap_gb300.build`` or ``build()``.
+Usage: ``python combine_symmetric_heap_gb300/build.py`` or ``build()`` (this
+file is loaded by path so that building never imports the package, whose
+import requires the built library).
 Objects and the library go to ``combine_symmetric_heap_gb300/_build/``; a
 translation unit is recompiled only when it or a header is newer than its
 object.
