@@ -198,7 +198,8 @@ class SymHeap:
     def __init__(self, shape: dict, device="cuda", align: int = 0):
         self.shape = dict(shape)
         prs, total = sym_heap_bytes(shape, align)
-        self.buf = torch.empty(total + 256, dtype=torch.uint8, device=device)
+        # zeroed once: the status word and the fused-kernel counters start at 0
+        self.buf = torch.zeros(total + 256, dtype=torch.uint8, device=device)
         pad = (-self.buf.data_ptr()) % 256
         self.buf = self.buf[pad:pad + total]
         self.desc = sym_heap_init(shape, self.buf.data_ptr(), total, align)

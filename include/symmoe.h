@@ -131,8 +131,11 @@ int sym_heap_bytes(const moe_shape *s, uint64_t align, uint64_t *per_rank_size,
  * (collective "alloc + register" of the CCO guide, reduced to arithmetic:
  * same windows, same order, same offsets in every slot).
  *   dev_base: device pointer, 256-byte aligned, owned by the caller, at least
- *             sym_heap_bytes(...) bytes; the library keeps no reference other
- *             than the copy in *out.
+ *             sym_heap_bytes(...) bytes, whose contents are zero before the
+ *             first call that uses the heap (e.g. cudaMemsetAsync(dev_base, 0,
+ *             bytes)): the status word and the fused-kernel counters start
+ *             from zero.  The library keeps no reference other than the copy
+ *             in *out.
  *   out:      filled descriptor (epoch 0, wait_timeout_us 2,000,000).
  * Host only, no device access.  SYM_EINVAL on a bad shape or alignment,
  * SYM_ENOSPACE if bytes is too small.
