@@ -36,6 +36,10 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--config", default="mixtral")
     p.add_argument("--fused", action="store_true")
+    p.add_argument("--tokens-per-slot", type=int, default=0,
+                   help="override T (smaller cases for profiler captures)")
+    p.add_argument("--world", type=int, default=0, help="override W")
+    p.add_argument("--experts", type=int, default=0, help="override E")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -174,14 +178,15 @@ def oracle_sample_run(cfg: dict, tokens, weights: dict):
     return dt
 
 
-def sample_weights(cfg: dict, tokens, device):
-    """Fresh host copies of the experts the sample tokens route to."""
+def sample_weights(cfg: dict, tokens, device, skip=()):
+    """Fresh host copies of the experts the sample tokens route to (input
+    generation, outside any timed region)."""
     import numpy as np
     import moe_synth as ms
     import oracle
     idx, _ = oracle.route_topk(ms.logits_np(cfg, rows=tokens), cfg["topk"])
     out = {}
-    for e in sorted(set(idx.reshape(-1).tolist())):
+    for e in sorted(set(idx.reshape(-1).tolist()) - set(skip)):
         if device is not None:
             out[e] = tuple(ms.weight_expert_torch(cfg, nm, e, device).view(__import__("torch").int16)
                            .cpu().numpy().view(np.uint16) for nm in ("gate", "up", "down"))
@@ -197,22 +202,34 @@ def cores_used():
         return os.cpu_count() or 1
 
 
+def get_cfg(args) -> dict:
+    import moe_synth as ms
+    cfg = dict(ms.CONFIGS[args.config])
+    if args.tokens_per_slot:
+        cfg["tokens_per_slot"] = args.tokens_per_slot
+    if args.world:
+        cfg["world"] = args.world
+    if args.experts:
+        cfg["num_experts"] = args.experts
+    return cfg
+
+
 def run_reference(args):
     rank, world, local = dist_env()
     if rank != 0:
         return 0
     import numpy as np
     import torch
-    import moe_synth as ms
-    cfg = ms.CONFIGS[args.config]
+    cfg = get_cfg(args)
     dev = torch.device("cuda", local) if torch.cuda.is_available() else None
     per_step = int(os.environ.get("SYMMOE_REF_TOKENS", "8"))
     n = cfg["world"] * cfg["tokens_per_slot"]
     rng = np.random.default_rng(0)
     times = []
+    wts = {}
     for s in range(args.warmup + args.steps):
         tokens = np.sort(rng.choice(n, size=per_step, replace=False))
-        wts = sample_weights(cfg, tokens, dev)
+        wts.update(sample_weights(cfg, tokens, dev, skip=set(wts)))
         dt = oracle_sample_run(cfg, tokens, wts)
         if s >= args.warmup:
             times.append(dt)
@@ -248,7 +265,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cfg = ms.CONFIGS[args.config]
+    cfg = get_cfg(args)
     fused = 1 if args.fused else 0
     n, k, H = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"], cfg["hidden"]
 
