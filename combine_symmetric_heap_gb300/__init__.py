@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
         L.moe_pipeline.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                    ctypes.c_int, _vp]
         L.sym_heap_status.argtypes = [P(SymHeapDesc), P(_i32), ctypes.c_int, _vp]
+        L.moe_dispatch_layout_noalloc.argtypes = [P(MoeShape), _vp, _vp, _vp, _vp, _vp, _vp]
         L.sym_strerror.argtypes = [ctypes.c_int]
         L.sym_strerror.restype = ctypes.c_char_p
         _lib = L
@@ -177,6 +178,15 @@ def moe_pipeline(heap: SymHeapDesc, logits, x, w_gate, w_up, w_down, idx, w, out
     _check(lib().moe_pipeline(ctypes.byref(heap), _ptr(logits), _ptr(x), _ptr(w_gate),
                               _ptr(w_up), _ptr(w_down), _ptr(idx), _ptr(w), _ptr(out),
                               int(fused), _stream(stream)), "moe_pipeline")
+
+
+def moe_dispatch_layout_noalloc(shape, idx, cnt, recv_off, total_recv, pos, stream=None) -> None:
+    """Dispatch layout from the routing indices alone, for callers that cannot
+    allocate device memory (its scratch is a library-owned device array)."""
+    s = _shape(dict(shape, hidden=shape.get("hidden", 128), inter=shape.get("inter", 128)))
+    _check(lib().moe_dispatch_layout_noalloc(ctypes.byref(s), _ptr(idx), _ptr(cnt), _ptr(recv_off),
+                                             _ptr(total_recv), _ptr(pos), _stream(stream)),
+           "moe_dispatch_layout_noalloc")
 
 
 def sym_heap_status(heap: SymHeapDesc, clear: bool = False, stream=None) -> int:

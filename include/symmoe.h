@@ -222,6 +222,38 @@ int moe_pipeline(sym_heap *h, const float *logits, const uint16_t *x, const uint
  */
 int sym_heap_status(const sym_heap *h, int32_t *status, int clear, symmoe_stream_t stream);
 
+/*
+ * moe_dispatch_layout_noalloc: the dispatch layout without a heap, for
+ * callers that cannot allocate device memory (a plug-in whose host framework
+ * hands it only its input and output buffers and owns every allocation, or a
+ * process that fixes its device-memory footprint at start-up).  The pages
+ * have no counterpart: their dispatch always runs on a registered window.
+ * Computes, from the routing indices alone, what moe_dispatch writes into the
+ * heap's signal area and pos windows:
+ *   idx:        device [N][k] int32, N = world * tokens_per_slot; every index
+ *               in [0, E) and the k of a token distinct (an index outside
+ *               [0, E) is not counted and gets pos -1);
+ *   cnt:        device [E] int32 (out): pairs per expert;
+ *   recv_off:   device [E] int32 (out): first receive row of each expert in
+ *               its slot;
+ *   total_recv: device [W] int32 (out): rows each slot receives;
+ *   pos:        device [N][k] int32 (out): receive row of every pair in its
+ *               destination slot, in the same order as moe_dispatch.
+ * Only s->world, tokens_per_slot, num_experts and topk are used.
+ * Scratch: a library-owned __device__ array of SYM_NOALLOC_HIST_MAX int32
+ * (1 MiB, on every device that loads the library, until exit) holding the
+ * E * ceil(N/128) chunk histograms; larger shapes return SYM_ENOSPACE.  The
+ * call makes no device allocation.  Its first call on a device looks up the
+ * array's address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  All calls share the array: calls
+ * that overlap on the GPU race on it and give wrong results.
+ * Asynchronous on `stream`; SYM_OK, SYM_EINVAL, SYM_ENOSPACE or SYM_ECUDA.
+ */
+#define SYM_NOALLOC_HIST_MAX (1 << 18)
+int moe_dispatch_layout_noalloc(const moe_shape *s, const int32_t *idx, int32_t *cnt,
+                                int32_t *recv_off, int32_t *total_recv, int32_t *pos,
+                                symmoe_stream_t stream);
+
 /* Static description of a SYM_* code (never NULL). */
 const char *sym_strerror(int code);
 
