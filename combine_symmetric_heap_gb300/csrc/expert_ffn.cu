@@ -10,9 +10,11 @@
 //
 // Tiling ("swap AB"): the tensor-core M side (128) runs over weight rows
 // (output features) and the N side over tokens, so an expert's ragged row
-// count only pads the N side of its last tile.  GEMM1 issues two MMAs per
-// K step that share the token tile: gate rows and up rows into two TMEM
-// accumulators, so silu(gate) * up is a per-thread epilogue.
+// count only shortens the N of its last tile's MMAs (rounded up to 16).
+// GEMM1 issues two MMAs per K step that share the token tile: gate rows and
+// up rows into two TMEM accumulators, so silu(gate) * up is a per-thread
+// epilogue.  (Putting 64 gate + 64 up rows on one M=128 MMA with N=256 and
+// swapping halves between warps measured 10-25% slower on GB300.)
 //
 // One persistent CTA per SM, warp-specialised:
 //   warp 0   TMA producer (one thread): waits for the dispatch ready counters
@@ -224,12 +226,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else if (wid == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int abuf = 0;
       uint32_t aphase = 0;
       for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+        // a ragged last token tile runs a narrower MMA (N rounded up to 16)
+        const TileInfo ti = decode_tile(h, prefix, cnt_s, roff_s, t, args.nf, BN);
+        const uint32_t idesc = idesc_bf16_f32(BM, min(BN, (ti.valid + 15) & ~15));
         if (!wait_or_stop(&acc_empty[abuf], aphase ^ 1u, t, stop_tile, abort_flag, tmo, h)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(abuf * C::ACC_COLS);

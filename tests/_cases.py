@@ -21,6 +21,8 @@ SMALL = {
     "many": dict(world=4, tokens_per_slot=96, hidden=128, num_experts=16, topk=4, inter=128),
     # one slot holding every expert, k = E (every expert receives every token)
     "allk": dict(world=1, tokens_per_slot=130, hidden=128, num_experts=8, topk=8, inter=256),
+    # k = 1, ~300 rows per expert: two token tiles (256 + ragged) per expert
+    "multi": dict(world=1, tokens_per_slot=600, hidden=128, num_experts=2, topk=1, inter=256),
 }
 
 

@@ -218,7 +218,8 @@ def _integer_case(world, tokens, hidden, inter, experts, k):
     return x, wg, wu, wd, idx, w, y_tok, out
 
 
-@pytest.mark.parametrize("shape", [(2, 64, 128, 256, 4, 2), (2, 150, 256, 128, 8, 2)])
+@pytest.mark.parametrize("shape", [(2, 64, 128, 256, 4, 2), (2, 150, 256, 128, 8, 2),
+                                   (1, 700, 128, 128, 2, 2)])
 def test_expert_ffn_integer_bit_exact(sm, shape):
     world, tokens, hidden, inter, experts, k = shape
     cfg = dict(world=world, tokens_per_slot=tokens, hidden=hidden, inter=inter,
