@@ -21,6 +21,7 @@ cudaError_t launch_expert_ffn(const sym_heap &h, const uint16_t *wg, const uint1
                               const uint16_t *wd, int num_sms, int wait_ready, cudaStream_t st);
 cudaError_t launch_combine(const sym_heap &h, const uint16_t *expert_out, const int32_t *idx,
                            const float *w, uint16_t *out, int num_sms, cudaStream_t st);
+size_t fused_ctrl_bytes(const moe_shape &s);
 cudaError_t launch_fused(const sym_heap &h, const float *logits, const uint16_t *x,
                          const uint16_t *wg, const uint16_t *wu, const uint16_t *wd,
                          int32_t *idx, float *w, uint16_t *out, int num_sms, cudaStream_t st);
@@ -84,7 +85,7 @@ Layout layout_of(const moe_shape *s) {
   L.off_status = take(4);
   L.off_ready = take((uint64_t)L.num_ready * 4);
   L.off_hist = take(E * nchunks * 4);
-  L.off_ctrl = take(256);
+  L.off_ctrl = take(fused_ctrl_bytes(*s));
   L.used = o;
   return L;
 }

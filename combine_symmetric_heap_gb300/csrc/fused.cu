@@ -1,10 +1,653 @@
-// fused.cu -- persistent single-launch pipeline (placeholder until built).
-#include "symmoe_dev.cuh"
+// fused.cu -- the whole MoE pipeline in one persistent launch.
+//
+// MORI CCO blog, "Mega-MoE: mega-kernel co-design with FlyDSL": dispatch,
+// expert GEMM and combine fused into a single kernel, removing the
+// synchronisation between kernels; and "In-kernel compute-communication
+// fusion": compute and data movement overlap at tile granularity inside one
+// launch.  Here the four stages run in one launch and overlap per tile:
+//
+//   phase 1  route + count, one task per 128-token chunk: route the chunk,
+//            then per-expert bitmasks give every pair its rank in the chunk
+//            and the chunk histogram.  The CTA that completes the last chunk
+//            runs the scan (counts, receive offsets, totals) and clears the
+//            readiness counters, then publishes scan_done = epoch.
+//   phase 2  scatter, one warp per token: rows go straight into the
+//            destination slot's recv_x window; each row raises the ready
+//            counter of its 128-row block (release).
+//   phase 3  expert GEMM tiles, pulled one at a time by each CTA's TMA
+//            producer from two counters (all gate/up tiles first, then down
+//            tiles) and handed to the MMA and epilogue warps through a
+//            shared-memory tile queue.  A gate/up tile starts once the ready
+//            counters of its token rows are complete; a down tile once every
+//            gate/up feature tile of its token rows has finished (h_ready);
+//            each epilogue warp bumps h_ready / y_ready of the tile's token
+//            block once its quarter of the tile is stored.
+//   phase 4  combine, one warp per token, each pair gated on y_ready.
+//
+// Forward progress: work is claimed from per-phase counters and a CTA moves to
+// a phase only after it found the previous phase's counter exhausted, so a
+// task only waits for tasks of earlier phases, all of which have been claimed
+// by running CTAs; every wait is also bounded by the heap's wait_timeout_us
+// (on expiry: SYM_STATUS_TIMEOUT, a global abort flag, and every CTA skips
+// the rest of its work).  The last CTA to exit resets the counters, so the
+// next launch on the stream starts clean.
+#include "gemm_core.cuh"
 
 namespace symmoe {
-cudaError_t launch_fused(const sym_heap &, const float *, const uint16_t *, const uint16_t *,
-                         const uint16_t *, const uint16_t *, int32_t *, float *, uint16_t *, int,
-                         cudaStream_t) {
-  return cudaErrorNotSupported;
+
+using gemm::TileInfo;
+
+constexpr int FUSED_THREADS = 256;  // warps 0-5 run the GEMM roles, all 8 the memory phases
+constexpr int FUSED_CHUNK = SYM_COUNT_CHUNK;
+constexpr int SCATTER_TOKENS = 8;  // tokens per scatter task (one warp each)
+constexpr int COMBINE_TOKENS = 8;  // tokens per combine task
+constexpr int TQ = 8;              // tile queue depth
+constexpr int FUSED_CTRL_SMEM = 512;
+
+// control words in slot 0's ctrl window
+enum Ctl : int {
+  C_ROUTE_NEXT = 0,
+  C_ROUTE_DONE = 1,
+  C_SCAN_DONE = 2,  // epoch of the last completed scan
+  C_SCATTER_NEXT = 3,
+  C_G1_NEXT = 4,
+  C_G2_NEXT = 5,
+  C_COMB_NEXT = 6,
+  C_EXIT = 7,
+  C_ABORT = 8,
+  C_WORDS = 64
+};
+
+__host__ __device__ inline int fused_h_blocks(const moe_shape &s) {
+  return s.world * s.tokens_per_slot * s.topk / 128 + s.num_experts + 1;
 }
+__host__ __device__ inline int fused_y_blocks(const moe_shape &s) {
+  return s.world * s.tokens_per_slot * s.topk / 256 + s.num_experts + 1;
+}
+
+struct FusedArgs {
+  const float *logits;
+  const uint16_t *x;
+  int32_t *idx;
+  float *w;
+  uint16_t *out;
+};
+
+__device__ __forceinline__ uint32_t *ctl(const sym_heap &h) { return win<uint32_t>(h, 0, h.off_ctrl); }
+__device__ __forceinline__ uint32_t *h_ready(const sym_heap &h) { return ctl(h) + C_WORDS; }
+__device__ __forceinline__ uint32_t *y_ready(const sym_heap &h) {
+  return ctl(h) + C_WORDS + fused_h_blocks(h.s);
+}
+__device__ __forceinline__ bool global_abort(const sym_heap &h) {
+  return *reinterpret_cast<volatile uint32_t *>(ctl(h) + C_ABORT) != 0;
+}
+__device__ __forceinline__ void set_abort(const sym_heap &h) {
+  raise_status(h, SYM_STATUS_TIMEOUT);
+  atomicExch(ctl(h) + C_ABORT, 1u);
+}
+
+// Bounded acquire-wait until *p >= target; gives up on timeout (setting the
+// global abort) or when another CTA aborted.
+__device__ inline bool wait_geq(const sym_heap &h, const uint32_t *p, uint32_t target) {
+  if (ld_acquire_u32(p) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = (uint64_t)h.wait_timeout_us * 1000ull;
+  for (uint32_t it = 0;; ++it) {
+    if (ld_acquire_u32(p) >= target) return true;
+    if (global_abort(h)) return false;
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > limit) {
+      set_abort(h);
+      return false;
+    }
+    __nanosleep(128);
+  }
+}
+
+// Claim the next task of a phase (thread 0), broadcast to the CTA.
+__device__ inline int claim(const sym_heap &h, int counter, int *bcast) {
+  __syncthreads();
+  if (threadIdx.x == 0) *bcast = global_abort(h) ? 0x7fffffff : (int)atomicAdd(ctl(h) + counter, 1u);
+  __syncthreads();
+  return *bcast;
+}
+
+// ---------------------------------------------------------------- phase 1
+// Top-k of one token by one warp (k passes over the row; the row is L1-hot).
+__device__ inline void route_token(const float *__restrict__ row, int E, int k, int32_t *idx_out,
+                                   float *w_out, int lane) {
+  float my_val = -INFINITY;  // lane j keeps the j-th selected logit
+  int my_idx = -1;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+    for (int e0 = 0; e0 < E; e0 += 32) {  // uniform trip count across the warp
+      const int e = e0 + lane;
+      bool used = false;  // selected in an earlier round
+      for (int j = 0; j < r; ++j) used |= (__shfl_sync(0xffffffffu, my_idx, j) == e);
+      if (e < E && !used) {
+        const float v = __ldg(row + e);
+        if (v > bv || be == 0x7fffffff) {
+          bv = v;
+          be = e;
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if (lane == r) {
+      my_val = bv;
+      my_idx = be;
+    }
+  }
+  const float top = __shfl_sync(0xffffffffu, my_val, 0);
+  const float z = lane < k ? expf(my_val - top) : 0.f;
+  float s = z;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane < k) {
+    idx_out[lane] = my_idx;
+    w_out[lane] = z / s;
+  }
+}
+
+__device__ inline void route_count_chunk(const sym_heap &h, const FusedArgs &a, int chunk,
+                                         uint32_t *mask) {
+  const int E = h.s.num_experts, k = h.s.topk, T = h.s.tokens_per_slot;
+  const int N = h.s.world * T;
+  const int nchunks = (N + FUSED_CHUNK - 1) / FUSED_CHUNK;
+  const int wid = warp_id(), lane = lane_id(), nw = blockDim.x >> 5;
+  for (int t = wid; t < FUSED_CHUNK; t += nw) {
+    const int g = chunk * FUSED_CHUNK + t;
+    if (g < N)
+      route_token(a.logits + (size_t)g * E, E, k, a.idx + (size_t)g * k, a.w + (size_t)g * k, lane);
+  }
+  for (int i = threadIdx.x; i < E * (FUSED_CHUNK / 32); i += blockDim.x) mask[i] = 0;
+  __syncthreads();
+  const int t = threadIdx.x;
+  const int g = chunk * FUSED_CHUNK + t;
+  const uint32_t bit = 1u << (t & 31);
+  const int word = t >> 5;
+  if (t < FUSED_CHUNK && g < N) {
+    for (int j = 0; j < k; ++j) {
+      const int e = a.idx[(size_t)g * k + j];
+      if (atomicOr(&mask[e * (FUSED_CHUNK / 32) + word], bit) & bit)
+        raise_status(h, SYM_STATUS_OVERFLOW);
+    }
+  }
+  __syncthreads();
+  if (t < FUSED_CHUNK && g < N) {
+    int32_t *pos = win<int32_t>(h, g / T, h.off_pos) + (size_t)(g % T) * k;
+    for (int j = 0; j < k; ++j) {
+      const int e = a.idx[(size_t)g * k + j];
+      const uint32_t *m = mask + e * (FUSED_CHUNK / 32);
+      int r = __popc(m[word] & (bit - 1u));
+      for (int w = 0; w < word; ++w) r += __popc(m[w]);
+      pos[j] = r;
+    }
+  }
+  int32_t *hist = win<int32_t>(h, 0, h.off_hist);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const uint32_t *m = mask + e * (FUSED_CHUNK / 32);
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < FUSED_CHUNK / 32; ++w) c += __popc(m[w]);
+    hist[(size_t)e * nchunks + chunk] = c;
+  }
+}
+
+// The scan, run by the CTA that completed the last chunk.
+__device__ inline void scan_and_publish(const sym_heap &h, int32_t *cnt_s) {
+  const int E = h.s.num_experts, W = h.s.world, E_loc = E / W;
+  const int N = W * h.s.tokens_per_slot;
+  const int nchunks = (N + FUSED_CHUNK - 1) / FUSED_CHUNK;
+  int32_t *hist = win<int32_t>(h, 0, h.off_hist);
+  const int lane = lane_id(), wid = warp_id(), nw = blockDim.x >> 5;
+  __threadfence();
+  for (int e = wid; e < E; e += nw) {
+    int32_t *row = hist + (size_t)e * nchunks;
+    int carry = 0;
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c < nchunks ? __ldcg(row + c) : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (c < nchunks) row[c] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) cnt_s[e] = carry;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int d = e / E_loc, l = e % E_loc;
+    int off = 0;
+    for (int i = 0; i < l; ++i) off += cnt_s[d * E_loc + i];
+    win<int32_t>(h, d, h.off_cnt)[l] = cnt_s[e];
+    win<int32_t>(h, d, h.off_recv_off)[l] = off;
+    if (l == E_loc - 1) *win<int32_t>(h, d, h.off_total) = off + cnt_s[e];
+  }
+  for (int i = threadIdx.x; i < W * (int)h.num_ready; i += blockDim.x)
+    win<uint32_t>(h, i / h.num_ready, h.off_ready)[i % h.num_ready] = 0u;
+  const int nh = fused_h_blocks(h.s), ny = fused_y_blocks(h.s);
+  for (int i = threadIdx.x; i < nh; i += blockDim.x) h_ready(h)[i] = 0u;
+  for (int i = threadIdx.x; i < ny; i += blockDim.x) y_ready(h)[i] = 0u;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicExch(ctl(h) + C_SCAN_DONE, h.epoch);
+  }
+}
+
+// ---------------------------------------------------------------- phase 2
+// One warp per token; dst_s is this warp's 32-entry destination table.
+__device__ inline void scatter_token(const sym_heap &h, const FusedArgs &a, int g, int lane,
+                                     uint4 **dst_s) {
+  const int E = h.s.num_experts, k = h.s.topk, T = h.s.tokens_per_slot, H = h.s.hidden;
+  const int E_loc = E / h.s.world;
+  const int N = h.s.world * T;
+  const int nchunks = (N + FUSED_CHUNK - 1) / FUSED_CHUNK;
+  int32_t *pos = win<int32_t>(h, g / T, h.off_pos) + (size_t)(g % T) * k;
+  int d = 0, p = -1;
+  if (lane < k) {
+    const int e = __ldcg(a.idx + (size_t)g * k + lane);
+    d = e / E_loc;
+    p = __ldcg(win<int32_t>(h, d, h.off_recv_off) + e % E_loc) +
+        __ldcg(win<int32_t>(h, 0, h.off_hist) + (size_t)e * nchunks + g / FUSED_CHUNK) +
+        __ldcg(pos + lane);
+    uint4 *dst = nullptr;
+    if (p < 0 || (uint64_t)p >= h.cap) {
+      raise_status(h, SYM_STATUS_OVERFLOW);
+      p = -1;
+    } else {
+      dst = win<uint4>(h, d, h.off_recv_x) + (size_t)p * (H / 8);
+    }
+    pos[lane] = p;
+    dst_s[lane] = dst;
+  }
+  __syncwarp();
+  const uint4 *src = reinterpret_cast<const uint4 *>(a.x) + (size_t)g * (H / 8);
+  for (int c = lane; c < H / 8; c += 32) {
+    const uint4 v = __ldg(src + c);
+    for (int j = 0; j < k; ++j)
+      if (dst_s[j]) dst_s[j][c] = v;
+  }
+  if (lane < k && p >= 0) {
+    win<int32_t>(h, d, h.off_recv_pair)[p] = g * k + lane;
+    win<float>(h, d, h.off_recv_w)[p] = __ldcg(a.w + (size_t)g * k + lane);
+  }
+  // the rows are read next by TMA (async proxy) in other CTAs
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __threadfence();
+  __syncwarp();
+  if (lane < k && p >= 0) atomicAdd(win<uint32_t>(h, d, h.off_ready) + p / SYM_ROWS_PER_FLAG, 1u);
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------- phase 4
+// One warp per token; src_s / w_s are this warp's 32-entry tables.
+__device__ inline void combine_token(const sym_heap &h, const FusedArgs &a, const gemm::Tables &tb,
+                                     int g, int lane, const uint4 **src_s, float *w_s) {
+  const int E = h.s.num_experts, k = h.s.topk, T = h.s.tokens_per_slot, H = h.s.hidden;
+  const int E_loc = E / h.s.world;
+  const int nf2 = gemm::nf_of(h, gemm::DOWN);
+  bool ok = true;
+  if (lane < k) {
+    const int e = __ldcg(a.idx + (size_t)g * k + lane);
+    const int p = __ldcg(win<const int32_t>(h, g / T, h.off_pos) + (size_t)(g % T) * k + lane);
+    const uint4 *src = nullptr;
+    if (p >= 0) {
+      // the 256-row down tile holding this row: all 4 epilogue warps of
+      // every feature tile have stored it
+      const int blk = tb.prefix(gemm::DOWN)[e] / nf2 + (p - tb.roff[e]) / 256;
+      ok = wait_geq(h, y_ready(h) + blk, 4u * (uint32_t)nf2);
+      src = win<const uint4>(h, e / E_loc, h.off_y) + (size_t)p * (H / 8);
+    }
+    src_s[lane] = src;
+    w_s[lane] = __ldcg(a.w + (size_t)g * k + lane);
+  }
+  if (!__all_sync(0xffffffffu, ok)) return;
+  uint4 *dst = reinterpret_cast<uint4 *>(a.out) + (size_t)g * (H / 8);
+  for (int c = lane; c < H / 8; c += 32) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const uint4 *sj = src_s[j];
+      if (!sj) continue;
+      const float ww = w_s[j];
+      const uint4 v = __ldcg(sj + c);
+      acc[0] = fmaf(ww, bf16lo(v.x), acc[0]);
+      acc[1] = fmaf(ww, bf16hi(v.x), acc[1]);
+      acc[2] = fmaf(ww, bf16lo(v.y), acc[2]);
+      acc[3] = fmaf(ww, bf16hi(v.y), acc[3]);
+      acc[4] = fmaf(ww, bf16lo(v.z), acc[4]);
+      acc[5] = fmaf(ww, bf16hi(v.z), acc[5]);
+      acc[6] = fmaf(ww, bf16lo(v.w), acc[6]);
+      acc[7] = fmaf(ww, bf16hi(v.w), acc[7]);
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    dst[c] = o;
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------- kernel
+__global__ void __launch_bounds__(FUSED_THREADS, 1)
+    moe_fused_kernel(const sym_heap h, const FusedArgs a, const __grid_constant__ CUtensorMap tm_g,
+                     const __grid_constant__ CUtensorMap tm_u,
+                     const __grid_constant__ CUtensorMap tm_rx,
+                     const __grid_constant__ CUtensorMap tm_d,
+                     const __grid_constant__ CUtensorMap tm_h) {
+  using namespace gemm;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *ring = smem;
+  uint8_t *ctrl_s = smem + (size_t)STAGES * STAGE_BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(ctrl_s);
+  uint64_t *empty = full + STAGES;
+  uint64_t *acc_full = empty + STAGES;
+  uint64_t *acc_empty = acc_full + 2;
+  uint64_t *tq_full = acc_empty + 2;
+  uint64_t *tq_empty = tq_full + TQ;
+  int2 *tq = reinterpret_cast<int2 *>(tq_empty + TQ);
+  uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(tq + TQ);
+  volatile int *abort_s = reinterpret_cast<volatile int *>(tmem_base_s + 1);
+  volatile int *stop_s = abort_s + 1;  // unused by the queue protocol (kept at INT_MAX)
+  int *bcast = const_cast<int *>(stop_s + 1);
+  const int E = h.s.num_experts;
+  int *tab = reinterpret_cast<int *>(ctrl_s + FUSED_CTRL_SMEM);
+  const Tables tb{tab, tab + E, tab + 2 * E, tab + 3 * E + 1};
+  const int wid = warp_id(), lane = lane_id();
+  // per-warp destination / source pointer and weight tables (32 entries each)
+  uint8_t *warp_tab = ctrl_s + FUSED_CTRL_SMEM + ((tables_bytes(E) + 15) & ~size_t(15));
+  void **ptr_s = reinterpret_cast<void **>(warp_tab) + wid * 32;
+  float *wgt_s = reinterpret_cast<float *>(warp_tab + FUSED_THREADS / 32 * 32 * sizeof(void *)) + wid * 32;
+  const uint32_t tmo = h.wait_timeout_us;
+  const int N = h.s.world * h.s.tokens_per_slot, k = h.s.topk;
+  const int nchunks = (N + FUSED_CHUNK - 1) / FUSED_CHUNK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    for (int i = 0; i < TQ; ++i) {
+      mbar_init(&tq_full[i], 1);
+      mbar_init(&tq_empty[i], 5);  // MMA thread + 4 epilogue warps
+    }
+    *abort_s = 0;
+    *stop_s = 0x7fffffff;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_g);
+    tma_prefetch_desc(&tm_u);
+    tma_prefetch_desc(&tm_rx);
+    tma_prefetch_desc(&tm_d);
+    tma_prefetch_desc(&tm_h);
+  }
+  if (wid == 1) {
+    tmem_alloc(tmem_base_s, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_s;
+
+  // ---------------- phase 1: route + count (the last finisher scans)
+  for (;;) {
+    const int c = claim(h, C_ROUTE_NEXT, bcast);
+    if (c >= nchunks) break;
+    route_count_chunk(h, a, c, reinterpret_cast<uint32_t *>(ring));
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *bcast = (int)atomicAdd(ctl(h) + C_ROUTE_DONE, 1u);
+    __syncthreads();
+    if (*bcast == nchunks - 1) scan_and_publish(h, reinterpret_cast<int32_t *>(ring));
+  }
+
+  // ---------------- phase 2: scatter
+  if (threadIdx.x == 0) *bcast = wait_geq(h, ctl(h) + C_SCAN_DONE, h.epoch) ? 1 : 0;
+  __syncthreads();
+  const bool scanned = *bcast != 0 && ld_acquire_u32(ctl(h) + C_SCAN_DONE) == h.epoch;
+  if (scanned) {
+    const int ntask = (N + SCATTER_TOKENS - 1) / SCATTER_TOKENS;
+    for (;;) {
+      const int t = claim(h, C_SCATTER_NEXT, bcast);
+      if (t >= ntask) break;
+      for (int i = wid; i < SCATTER_TOKENS; i += FUSED_THREADS / 32) {
+        const int g = t * SCATTER_TOKENS + i;
+        if (g < N) scatter_token(h, a, g, lane, reinterpret_cast<uint4 **>(ptr_s));
+      }
+    }
+  }
+
+  // ---------------- phase 3: expert GEMM tiles
+  if (scanned) build_tables(h, tb);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (scanned) {
+    const int total1 = tb.prefix(GATE_UP)[E], total2 = tb.prefix(DOWN)[E];
+    const int nf1 = nf_of(h, GATE_UP), nf2 = nf_of(h, DOWN);
+    if (wid == 0) {
+      if (lane == 0) {
+        // producer: claims tiles, gates them on their inputs, streams K blocks
+        int stage = 0, qs = 0;
+        uint32_t phase = 0, qphase = 0;
+        int kind = GATE_UP;
+        for (;;) {
+          int t = 0x7fffffff;
+          while (!*abort_s) {
+            if (kind == GATE_UP) {
+              t = global_abort(h) ? total1 : (int)atomicAdd(ctl(h) + C_G1_NEXT, 1u);
+              if (t < total1) break;
+              kind = DOWN;
+            } else {
+              t = global_abort(h) ? total2 : (int)atomicAdd(ctl(h) + C_G2_NEXT, 1u);
+              if (t >= total2) t = -1;  // sentinel: no more tiles
+              break;
+            }
+          }
+          if (*abort_s) t = -1;
+          if (!wait_or_stop(&tq_empty[qs], qphase ^ 1u, -1, stop_s, abort_s, tmo, h)) break;
+          tq[qs] = make_int2(kind, t);
+          mbar_arrive(&tq_full[qs]);
+          if (++qs == TQ) {
+            qs = 0;
+            qphase ^= 1u;
+          }
+          if (t < 0) break;
+          const TileInfo ti = decode(h, tb, kind, t);
+          bool ok;
+          if (kind == GATE_UP) {
+            ok = wait_rows_dispatched(h, ti, tmo, abort_s) && !global_abort(h);
+          } else {
+            // every gate/up feature tile of the (one or two) 128-row token
+            // blocks this 256-row tile covers
+            const int b1 = tb.prefix(GATE_UP)[ti.e] / nf1 + 2 * ti.n;
+            const int nb1 = (tb.cnt[ti.e] + 127) / 128;
+            ok = wait_geq(h, h_ready(h) + b1, 4u * (uint32_t)nf1);
+            if (ok && 2 * ti.n + 1 < nb1) ok = wait_geq(h, h_ready(h) + b1 + 1, 4u * (uint32_t)nf1);
+          }
+          if (!ok) {
+            set_abort(h);
+            *abort_s = 1;
+            break;
+          }
+          fence_proxy_async();
+          const Maps m = kind == GATE_UP ? Maps{&tm_g, &tm_u, &tm_rx} : Maps{&tm_d, &tm_d, &tm_h};
+          const int nk = nk_of(h, kind);
+          for (int kb = 0; kb < nk; ++kb) {
+            if (!wait_or_stop(&empty[stage], phase ^ 1u, -1, stop_s, abort_s, tmo, h)) break;
+            issue_loads(h, ti, m, kb, ring + (size_t)stage * STAGE_BYTES, &full[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+    } else if (wid == 1) {
+      if (lane == 0) {
+        // MMA issuer
+        int stage = 0, qs = 0, abuf = 0;
+        uint32_t phase = 0, qphase = 0, aphase = 0;
+        for (;;) {
+          if (!wait_or_stop(&tq_full[qs], qphase, -1, stop_s, abort_s, tmo, h)) break;
+          const int2 ent = tq[qs];
+          mbar_arrive(&tq_empty[qs]);
+          if (++qs == TQ) {
+            qs = 0;
+            qphase ^= 1u;
+          }
+          if (ent.y < 0) break;
+          const TileInfo ti = decode(h, tb, ent.x, ent.y);
+          if (!wait_or_stop(&acc_empty[abuf], aphase ^ 1u, -1, stop_s, abort_s, tmo, h)) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(abuf * ACC_COLS);
+          const int nk = nk_of(h, ti.kind);
+          bool stopped = false;
+          for (int kb = 0; kb < nk; ++kb) {
+            if (!wait_or_stop(&full[stage], phase, -1, stop_s, abort_s, tmo, h)) {
+              stopped = true;
+              break;
+            }
+            tc_fence_after();
+            issue_mmas(ti, ring + (size_t)stage * STAGE_BYTES, d_tmem, kb == 0);
+            tc_commit(&empty[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (stopped) break;
+          tc_commit(&acc_full[abuf]);
+          if (++abuf == 2) {
+            abuf = 0;
+            aphase ^= 1u;
+          }
+        }
+      }
+    } else if (wid < 6) {
+      // epilogue warps
+      const int q = wid & 3;
+      int qs = 0, abuf = 0;
+      uint32_t qphase = 0, aphase = 0;
+      for (;;) {
+        if (!wait_or_stop(&tq_full[qs], qphase, -1, stop_s, abort_s, tmo, h)) break;
+        const int2 ent = tq[qs];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tq_empty[qs]);
+        if (++qs == TQ) {
+          qs = 0;
+          qphase ^= 1u;
+        }
+        if (ent.y < 0) break;
+        const TileInfo ti = decode(h, tb, ent.x, ent.y);
+        if (!wait_or_stop(&acc_full[abuf], aphase, -1, stop_s, abort_s, tmo, h)) break;
+        tc_fence_after();
+        epilogue(h, ti, tmem_base, (uint32_t)(abuf * ACC_COLS), q, lane);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[abuf]);
+        if (++abuf == 2) {
+          abuf = 0;
+          aphase ^= 1u;
+        }
+        // publish this warp's quarter of the tile (a token block is complete
+        // when all 4 quarters of all its feature tiles are in)
+        __threadfence();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncwarp();
+        if (lane == 0)
+          atomicAdd((ti.kind == GATE_UP ? h_ready(h) : y_ready(h)) + token_block(h, tb, ti), 1u);
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---------------- phase 4: combine
+  if (scanned) {
+    const int ntask = (N + COMBINE_TOKENS - 1) / COMBINE_TOKENS;
+    for (;;) {
+      const int t = claim(h, C_COMB_NEXT, bcast);
+      if (t >= ntask) break;
+      for (int i = wid; i < COMBINE_TOKENS; i += FUSED_THREADS / 32) {
+        const int g = t * COMBINE_TOKENS + i;
+        if (g < N)
+          combine_token(h, a, tb, g, lane, reinterpret_cast<const uint4 **>(const_cast<const void **>(ptr_s)),
+                        wgt_s);
+      }
+    }
+  }
+
+  // ---------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (wid == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(ctl(h) + C_EXIT, 1u) == gridDim.x - 1) {
+      // last CTA out: reset the counters for the next launch
+      uint32_t *c = ctl(h);
+      c[C_ROUTE_NEXT] = 0;
+      c[C_ROUTE_DONE] = 0;
+      c[C_SCATTER_NEXT] = 0;
+      c[C_G1_NEXT] = 0;
+      c[C_G2_NEXT] = 0;
+      c[C_COMB_NEXT] = 0;
+      c[C_ABORT] = 0;
+      __threadfence();
+      c[C_EXIT] = 0;
+    }
+  }
+  (void)k;
+}
+
+size_t fused_ctrl_bytes(const moe_shape &s) {
+  return (size_t)(C_WORDS + fused_h_blocks(s) + fused_y_blocks(s)) * 4;
+}
+
+cudaError_t launch_fused(const sym_heap &h, const float *logits, const uint16_t *x,
+                         const uint16_t *wg, const uint16_t *wu, const uint16_t *wd, int32_t *idx,
+                         float *w, uint16_t *out, int num_sms, cudaStream_t st) {
+  using namespace gemm;
+  const int E = h.s.num_experts, H = h.s.hidden, I = h.s.inter;
+  CUtensorMap tg, tu, trx, td, th;
+  if (!encode_2d(&tg, wg, (uint64_t)E * I, H, BM) || !encode_2d(&tu, wu, (uint64_t)E * I, H, BM) ||
+      !encode_heap_3d(&trx, h, h.off_recv_x, H, K<GATE_UP>::BN) ||
+      !encode_2d(&td, wd, (uint64_t)E * H, I, BM) || !encode_heap_3d(&th, h, h.off_h, I, K<DOWN>::BN))
+    return cudaErrorInvalidValue;
+  const size_t smem = 1024 + (size_t)STAGES * STAGE_BYTES + FUSED_CTRL_SMEM +
+                      ((tables_bytes(E) + 15) & ~size_t(15)) +
+                      FUSED_THREADS / 32 * 32 * (sizeof(void *) + sizeof(float));
+  cudaError_t err = cudaFuncSetAttribute(moe_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+  if (err != cudaSuccess) return err;
+  const FusedArgs a{logits, x, idx, w, out};
+  moe_fused_kernel<<<num_sms, FUSED_THREADS, smem, st>>>(h, a, tg, tu, trx, td, th);
+  return cudaGetLastError();
+}
+
 }  // namespace symmoe
