@@ -64,7 +64,6 @@ Layout layout_of(const moe_shape *s) {
   const uint64_t W = s->world, T = s->tokens_per_slot, H = s->hidden, I = s->inter,
                  E = s->num_experts, k = s->topk;
   const uint64_t N = W * T, E_loc = E / W;
-  const uint64_t nchunks = (N + SYM_COUNT_CHUNK - 1) / SYM_COUNT_CHUNK;
   L.cap = N * (k < E_loc ? k : E_loc);
   L.num_ready = (uint32_t)((L.cap + SYM_ROWS_PER_FLAG - 1) / SYM_ROWS_PER_FLAG);
   uint64_t o = 0;
@@ -84,7 +83,9 @@ Layout layout_of(const moe_shape *s) {
   L.off_total = take(4);
   L.off_status = take(4);
   L.off_ready = take((uint64_t)L.num_ready * 4);
-  L.off_hist = take(E * nchunks * 4);
+  // chunk histograms: 128-token chunks for the stand-alone dispatch, 32-token
+  // chunks for the fused pipeline (the larger of the two)
+  L.off_hist = take(E * ((N + 31) / 32) * 4);
   L.off_ctrl = take(fused_ctrl_bytes(*s));
   L.used = o;
   return L;

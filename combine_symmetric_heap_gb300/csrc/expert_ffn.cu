@@ -91,19 +91,28 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (wid == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
+      // The readiness of tile i+1's rows is probed (without blocking) half way
+      // through tile i's K loop, so the acquire round trip hides behind the
+      // stages already in flight; only a tile whose rows are not ready yet
+      // waits at the tile boundary.
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
-        const TileInfo ti = decode(h, tb, KIND, t);
-        if (wait_ready) {
-          if (!wait_rows_dispatched(h, ti, tmo, abort_flag)) {
-            raise_status(h, SYM_STATUS_TIMEOUT);
-            *stop_tile = t;  // tiles >= t are not loaded; earlier ones finish
-            break;
-          }
-          fence_proxy_async();
+      int t = blockIdx.x;
+      bool ready_ok = true;
+      if (wait_ready && t < total_tiles) {
+        ready_ok = wait_rows_dispatched(h, decode(h, tb, KIND, t), tmo, abort_flag);
+        if (!ready_ok) {
+          raise_status(h, SYM_STATUS_TIMEOUT);
+          *stop_tile = t;
         }
+      }
+      while (ready_ok && t < total_tiles && !*abort_flag) {
+        if (wait_ready) fence_proxy_async();
+        const TileInfo ti = decode(h, tb, KIND, t);
+        const int t_next = t + gridDim.x;
+        bool next_ok = !wait_ready || t_next >= total_tiles;
         for (int kb = 0; kb < nk; ++kb) {
+          if (!next_ok && kb == nk / 2) next_ok = rows_dispatched_now(h, decode(h, tb, KIND, t_next));
           if (!wait_or_stop(&empty[stage], phase ^ 1u, -1, stop_tile, abort_flag, tmo, h)) break;
           issue_loads(h, ti, maps, kb, ring + (size_t)stage * STAGE_BYTES, &full[stage]);
           if (++stage == STAGES) {
@@ -111,6 +120,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             phase ^= 1u;
           }
         }
+        if (!next_ok && !wait_rows_dispatched(h, decode(h, tb, KIND, t_next), tmo, abort_flag)) {
+          raise_status(h, SYM_STATUS_TIMEOUT);
+          *stop_tile = t_next;  // tiles >= t_next are not loaded; earlier ones finish
+          break;
+        }
+        t = t_next;
       }
     }
   } else if (wid == 1) {

@@ -6,9 +6,9 @@
 // fusion": compute and data movement overlap at tile granularity inside one
 // launch.  Here the four stages run in one launch and overlap per tile:
 //
-//   phase 1  route + count, one task per 128-token chunk: route the chunk,
-//            then per-expert bitmasks give every pair its rank in the chunk
-//            and the chunk histogram.  The CTA that completes the last chunk
+//   phase 1  route + count, one task per 32-token chunk: route the chunk
+//            (logits rows staged in shared memory), then per-expert bitmasks
+//            give every pair its rank in the chunk and the chunk histogram.  The CTA that completes the last chunk
 //            runs the scan (counts, receive offsets, totals) and clears the
 //            readiness counters, then publishes scan_done = epoch.
 //   phase 2  scatter, one warp per token: rows go straight into the
@@ -38,7 +38,7 @@ namespace symmoe {
 using gemm::TileInfo;
 
 constexpr int FUSED_THREADS = 256;  // warps 0-5 run the GEMM roles, all 8 the memory phases
-constexpr int FUSED_CHUNK = SYM_COUNT_CHUNK;
+constexpr int FUSED_CHUNK = 32;  // tokens per route+count task (one bitmask word per expert)
 constexpr int SCATTER_TOKENS = 8;  // tokens per scatter task (one warp each)
 constexpr int COMBINE_TOKENS = 8;  // tokens per combine task
 constexpr int TQ = 8;              // tile queue depth
@@ -112,24 +112,20 @@ __device__ inline int claim(const sym_heap &h, int counter, int *bcast) {
 }
 
 // ---------------------------------------------------------------- phase 1
-// Top-k of one token by one warp (k passes over the row; the row is L1-hot).
-__device__ inline void route_token(const float *__restrict__ row, int E, int k, int32_t *idx_out,
-                                   float *w_out, int lane) {
+// Top-k of one token by one warp over its logits row staged in shared memory
+// (row[] is consumed: selected entries become -inf).
+__device__ inline void route_token(float *row, int E, int k, int32_t *idx_out, float *w_out,
+                                   int lane) {
   float my_val = -INFINITY;  // lane j keeps the j-th selected logit
   int my_idx = -1;
   for (int r = 0; r < k; ++r) {
     float bv = -INFINITY;
     int be = 0x7fffffff;
-    for (int e0 = 0; e0 < E; e0 += 32) {  // uniform trip count across the warp
-      const int e = e0 + lane;
-      bool used = false;  // selected in an earlier round
-      for (int j = 0; j < r; ++j) used |= (__shfl_sync(0xffffffffu, my_idx, j) == e);
-      if (e < E && !used) {
-        const float v = __ldg(row + e);
-        if (v > bv || be == 0x7fffffff) {
-          bv = v;
-          be = e;
-        }
+    for (int e = lane; e < E; e += 32) {  // ascending index: '>' keeps the lower one on ties
+      const float v = row[e];
+      if (v > bv || be == 0x7fffffff) {
+        bv = v;
+        be = e;
       }
     }
 #pragma unroll
@@ -141,6 +137,8 @@ __device__ inline void route_token(const float *__restrict__ row, int E, int k, 
         be = oe;
       }
     }
+    if (lane == (be & 31)) row[be] = -INFINITY;  // logits are finite: never picked again
+    __syncwarp();
     if (lane == r) {
       my_val = bv;
       my_idx = be;
@@ -157,49 +155,41 @@ __device__ inline void route_token(const float *__restrict__ row, int E, int k, 
   }
 }
 
+// Route the 32 tokens of a chunk (4 per warp), then rank each pair inside the
+// chunk by the per-expert bitmask and write the chunk histogram.
+// smem: 8 logits rows of E floats, then the E mask words.
 __device__ inline void route_count_chunk(const sym_heap &h, const FusedArgs &a, int chunk,
-                                         uint32_t *mask) {
+                                         float *smem) {
   const int E = h.s.num_experts, k = h.s.topk, T = h.s.tokens_per_slot;
   const int N = h.s.world * T;
   const int nchunks = (N + FUSED_CHUNK - 1) / FUSED_CHUNK;
   const int wid = warp_id(), lane = lane_id(), nw = blockDim.x >> 5;
+  float *row = smem + (size_t)wid * E;
+  uint32_t *mask = reinterpret_cast<uint32_t *>(smem + (size_t)nw * E);
   for (int t = wid; t < FUSED_CHUNK; t += nw) {
     const int g = chunk * FUSED_CHUNK + t;
-    if (g < N)
-      route_token(a.logits + (size_t)g * E, E, k, a.idx + (size_t)g * k, a.w + (size_t)g * k, lane);
+    if (g >= N) break;
+    const float *src = a.logits + (size_t)g * E;
+    for (int e = lane; e < E; e += 32) row[e] = __ldg(src + e);
+    __syncwarp();
+    route_token(row, E, k, a.idx + (size_t)g * k, a.w + (size_t)g * k, lane);
+    __syncwarp();
   }
-  for (int i = threadIdx.x; i < E * (FUSED_CHUNK / 32); i += blockDim.x) mask[i] = 0;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) mask[i] = 0;
   __syncthreads();
   const int t = threadIdx.x;
   const int g = chunk * FUSED_CHUNK + t;
-  const uint32_t bit = 1u << (t & 31);
-  const int word = t >> 5;
-  if (t < FUSED_CHUNK && g < N) {
-    for (int j = 0; j < k; ++j) {
-      const int e = a.idx[(size_t)g * k + j];
-      if (atomicOr(&mask[e * (FUSED_CHUNK / 32) + word], bit) & bit)
-        raise_status(h, SYM_STATUS_OVERFLOW);
-    }
-  }
+  const uint32_t bit = 1u << t;
+  if (t < FUSED_CHUNK && g < N)
+    for (int j = 0; j < k; ++j)
+      if (atomicOr(&mask[a.idx[(size_t)g * k + j]], bit) & bit) raise_status(h, SYM_STATUS_OVERFLOW);
   __syncthreads();
   if (t < FUSED_CHUNK && g < N) {
     int32_t *pos = win<int32_t>(h, g / T, h.off_pos) + (size_t)(g % T) * k;
-    for (int j = 0; j < k; ++j) {
-      const int e = a.idx[(size_t)g * k + j];
-      const uint32_t *m = mask + e * (FUSED_CHUNK / 32);
-      int r = __popc(m[word] & (bit - 1u));
-      for (int w = 0; w < word; ++w) r += __popc(m[w]);
-      pos[j] = r;
-    }
+    for (int j = 0; j < k; ++j) pos[j] = __popc(mask[a.idx[(size_t)g * k + j]] & (bit - 1u));
   }
   int32_t *hist = win<int32_t>(h, 0, h.off_hist);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const uint32_t *m = mask + e * (FUSED_CHUNK / 32);
-    int c = 0;
-#pragma unroll
-    for (int w = 0; w < FUSED_CHUNK / 32; ++w) c += __popc(m[w]);
-    hist[(size_t)e * nchunks + chunk] = c;
-  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)e * nchunks + chunk] = __popc(mask[e]);
 }
 
 // The scan, run by the CTA that completed the last chunk.
@@ -417,7 +407,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
   for (;;) {
     const int c = claim(h, C_ROUTE_NEXT, bcast);
     if (c >= nchunks) break;
-    route_count_chunk(h, a, c, reinterpret_cast<uint32_t *>(ring));
+    route_count_chunk(h, a, c, reinterpret_cast<float *>(ring));
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) *bcast = (int)atomicAdd(ctl(h) + C_ROUTE_DONE, 1u);
@@ -451,53 +441,73 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     const int nf1 = nf_of(h, GATE_UP), nf2 = nf_of(h, DOWN);
     if (wid == 0) {
       if (lane == 0) {
-        // producer: claims tiles, gates them on their inputs, streams K blocks
+        // producer: claims tiles, gates them on their inputs, streams K blocks.
+        // The claim of tile i+1 is issued at the start of tile i's K loop and
+        // its inputs are probed half way through, so neither round trip
+        // stalls the ring; a tile whose inputs are not ready yet waits at the
+        // tile boundary.
         int stage = 0, qs = 0;
         uint32_t phase = 0, qphase = 0;
         int kind = GATE_UP;
-        for (;;) {
-          int t = 0x7fffffff;
-          while (!*abort_s) {
-            if (kind == GATE_UP) {
-              t = global_abort(h) ? total1 : (int)atomicAdd(ctl(h) + C_G1_NEXT, 1u);
-              if (t < total1) break;
-              kind = DOWN;
-            } else {
-              t = global_abort(h) ? total2 : (int)atomicAdd(ctl(h) + C_G2_NEXT, 1u);
-              if (t >= total2) t = -1;  // sentinel: no more tiles
-              break;
-            }
+        auto deps_now = [&](const TileInfo &ti) -> bool {
+          if (ti.kind == GATE_UP) return rows_dispatched_now(h, ti);
+          const int b1 = tb.prefix(GATE_UP)[ti.e] / nf1 + 2 * ti.n;
+          const int nb1 = (tb.cnt[ti.e] + 127) / 128;
+          if (ld_acquire_u32(h_ready(h) + b1) < 4u * (uint32_t)nf1) return false;
+          return 2 * ti.n + 1 >= nb1 || ld_acquire_u32(h_ready(h) + b1 + 1) >= 4u * (uint32_t)nf1;
+        };
+        auto deps_wait = [&](const TileInfo &ti) -> bool {
+          if (ti.kind == GATE_UP) return wait_rows_dispatched(h, ti, tmo, abort_s) && !global_abort(h);
+          // every gate/up feature tile of the (one or two) 128-row token
+          // blocks this 256-row tile covers, all four epilogue quarters each
+          const int b1 = tb.prefix(GATE_UP)[ti.e] / nf1 + 2 * ti.n;
+          const int nb1 = (tb.cnt[ti.e] + 127) / 128;
+          bool ok = wait_geq(h, h_ready(h) + b1, 4u * (uint32_t)nf1);
+          if (ok && 2 * ti.n + 1 < nb1) ok = wait_geq(h, h_ready(h) + b1 + 1, 4u * (uint32_t)nf1);
+          return ok;
+        };
+        auto counter = [&](int kd) { return ctl(h) + (kd == GATE_UP ? C_G1_NEXT : C_G2_NEXT); };
+        // resolve a claimed ticket into (kind, tile) or the sentinel (-1)
+        auto resolve = [&](uint32_t ticket) -> int2 {
+          if (global_abort(h) || *abort_s) return make_int2(kind, -1);
+          if (kind == GATE_UP) {
+            if ((int)ticket < total1) return make_int2(GATE_UP, (int)ticket);
+            kind = DOWN;
+            ticket = atomicAdd(counter(DOWN), 1u);
           }
-          if (*abort_s) t = -1;
-          if (!wait_or_stop(&tq_empty[qs], qphase ^ 1u, -1, stop_s, abort_s, tmo, h)) break;
-          tq[qs] = make_int2(kind, t);
+          return make_int2(DOWN, (int)ticket < total2 ? (int)ticket : -1);
+        };
+        auto push = [&](int2 ent) -> bool {
+          if (!wait_or_stop(&tq_empty[qs], qphase ^ 1u, -1, stop_s, abort_s, tmo, h)) return false;
+          tq[qs] = ent;
           mbar_arrive(&tq_full[qs]);
           if (++qs == TQ) {
             qs = 0;
             qphase ^= 1u;
           }
-          if (t < 0) break;
-          const TileInfo ti = decode(h, tb, kind, t);
-          bool ok;
-          if (kind == GATE_UP) {
-            ok = wait_rows_dispatched(h, ti, tmo, abort_s) && !global_abort(h);
-          } else {
-            // every gate/up feature tile of the (one or two) 128-row token
-            // blocks this 256-row tile covers
-            const int b1 = tb.prefix(GATE_UP)[ti.e] / nf1 + 2 * ti.n;
-            const int nb1 = (tb.cnt[ti.e] + 127) / 128;
-            ok = wait_geq(h, h_ready(h) + b1, 4u * (uint32_t)nf1);
-            if (ok && 2 * ti.n + 1 < nb1) ok = wait_geq(h, h_ready(h) + b1 + 1, 4u * (uint32_t)nf1);
-          }
-          if (!ok) {
-            set_abort(h);
-            *abort_s = 1;
-            break;
-          }
+          return true;
+        };
+        int2 cur = resolve(atomicAdd(counter(kind), 1u));
+        bool ok = push(cur);
+        if (ok && cur.y >= 0 && !deps_wait(decode(h, tb, cur.x, cur.y))) {
+          set_abort(h);
+          *abort_s = 1;
+          ok = false;
+        }
+        while (ok && cur.y >= 0) {
           fence_proxy_async();
-          const Maps m = kind == GATE_UP ? Maps{&tm_g, &tm_u, &tm_rx} : Maps{&tm_d, &tm_d, &tm_h};
-          const int nk = nk_of(h, kind);
+          const TileInfo ti = decode(h, tb, cur.x, cur.y);
+          const Maps m = ti.kind == GATE_UP ? Maps{&tm_g, &tm_u, &tm_rx} : Maps{&tm_d, &tm_d, &tm_h};
+          const int nk = nk_of(h, ti.kind);
+          uint32_t ticket = 0;
+          int2 nxt = make_int2(kind, -1);
+          bool next_ok = false;
           for (int kb = 0; kb < nk; ++kb) {
+            if (kb == 0) ticket = atomicAdd(counter(kind), 1u);
+            if (kb == nk / 2) {
+              nxt = resolve(ticket);
+              next_ok = nxt.y < 0 || deps_now(decode(h, tb, nxt.x, nxt.y));
+            }
             if (!wait_or_stop(&empty[stage], phase ^ 1u, -1, stop_s, abort_s, tmo, h)) break;
             issue_loads(h, ti, m, kb, ring + (size_t)stage * STAGE_BYTES, &full[stage]);
             if (++stage == STAGES) {
@@ -505,6 +515,14 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
               phase ^= 1u;
             }
           }
+          if (*abort_s) break;
+          if (!push(nxt)) break;
+          if (nxt.y >= 0 && !next_ok && !deps_wait(decode(h, tb, nxt.x, nxt.y))) {
+            set_abort(h);
+            *abort_s = 1;
+            break;
+          }
+          cur = nxt;
         }
       }
     } else if (wid == 1) {

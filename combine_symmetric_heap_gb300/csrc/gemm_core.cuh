@@ -250,6 +250,17 @@ __device__ inline bool wait_rows_dispatched(const sym_heap &h, const TileInfo &t
   return true;
 }
 
+// Non-blocking probe of the same counters (one acquire load each).
+__device__ inline bool rows_dispatched_now(const sym_heap &h, const TileInfo &ti) {
+  const int total = *win<const int32_t>(h, ti.d, h.off_total);
+  const uint32_t *ready = win<const uint32_t>(h, ti.d, h.off_ready);
+  for (int b = ti.row0 / SYM_ROWS_PER_FLAG; b <= (ti.row0 + ti.valid - 1) / SYM_ROWS_PER_FLAG; ++b) {
+    const uint32_t target = (uint32_t)min(SYM_ROWS_PER_FLAG, total - b * SYM_ROWS_PER_FLAG);
+    if (ld_acquire_u32(ready + b) < target) return false;
+  }
+  return true;
+}
+
 }  // namespace gemm
 
 // Tensor-map encoders (expert_ffn.cu): a bf16 matrix [rows][cols] with a box

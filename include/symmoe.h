@@ -107,7 +107,7 @@ typedef struct sym_heap {
   uint64_t cap;           /* receive rows per slot = N * min(k, E/W)           */
   uint64_t off_recv_x, off_y, off_h, off_recv_pair, off_recv_w, off_pos;
   uint64_t off_cnt, off_recv_off, off_total, off_status, off_ready;
-  uint64_t off_hist;      /* [ceil(N/128)][E] int32                            */
+  uint64_t off_hist;      /* chunk histograms, E * ceil(N/32) int32            */
   uint64_t off_ctrl;      /* fused-kernel counters and per-tile readiness      */
   uint32_t num_ready;     /* ready counters per slot = ceil(cap / 128)         */
   uint32_t epoch;         /* bumped by every dispatch / pipeline call          */

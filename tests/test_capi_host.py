@@ -67,7 +67,7 @@ def test_heap_layout(name):
             (d.off_recv_pair, d.cap * 4), (d.off_recv_w, d.cap * 4), (d.off_pos, T * k * 4),
             (d.off_cnt, e_loc * 4), (d.off_recv_off, e_loc * 4), (d.off_total, 4),
             (d.off_status, 4), (d.off_ready, d.num_ready * 4),
-            (d.off_hist, cfg["num_experts"] * ((n + 127) // 128) * 4),
+            (d.off_hist, cfg["num_experts"] * ((n + 31) // 32) * 4),
             (d.off_ctrl, 4 * (64 + (n * k // 128 + cfg["num_experts"] + 1)
                               + (n * k // 256 + cfg["num_experts"] + 1)))]
     for (o, b), (o2, _) in zip(wins, wins[1:]):
