@@ -54,6 +54,17 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The slowest rank's time (every rank gets it)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def workload_config(name: str, cfg: dict, fused: bool) -> dict:
     import moe_synth as ms
     n = cfg["world"] * cfg["tokens_per_slot"]
@@ -308,11 +319,7 @@ def run_ours(args):
         ev1.record(stream)
         torch.cuda.synchronize()
     barrier()
-    ms_total = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     assert heap.status(stream=stream) == 0, "device status word set during the timed steps"
     ms_step = ms_total / args.steps
     value = n * args.steps * world / (ms_total / 1e3)
@@ -409,11 +416,7 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
         e2e = {"value": n * e_steps * world / (e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": lg_h.numel() * 4 + x_h.numel() * 2,
                "d2h_bytes_per_step": out_h.numel() * 2, "steps": e_steps}

@@ -1,0 +1,115 @@
+"""Edge cases of the CUDA path against the oracle, staged and fused: every pair
+on two experts (all others empty), the largest E and k the ABI accepts, a
+single expert, token counts that are not multiples of any tile or chunk."""
+import numpy as np
+import pytest
+import torch
+
+import moe_synth as ms
+import oracle
+from _cases import assert_close, bf16_f64, bits, device_inputs, fresh_weight_fn
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def sm():
+    import combine_symmetric_heap_gb300 as m
+    return m
+
+
+def _oracle_from_idx(cfg, idx, w, wfn):
+    """The oracle's dispatch -> expert -> combine for a given routing."""
+    E, W, k = cfg["num_experts"], cfg["world"], cfg["topk"]
+    cnt, off, tot = oracle.count_experts(idx, E, W)
+    pos, rp, rw = oracle.place_pairs(idx, w, E, W)
+    rx = oracle.dispatch_rows(ms.x_np(cfg), rp, k)
+    h, y, ye = oracle.expert_ffn(rx, cnt, off, E, W, wfn)
+    out = oracle.combine(y, idx, w, pos, E, W)
+    return dict(cnt=cnt, off=off, tot=tot, pos=pos, y=y, y_exact=ye, out=out)
+
+
+def _run(sm, cfg, idx_np, w_np, fused):
+    logits, x, wg, wu, wd = device_inputs(cfg, DEV)
+    n, k = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"]
+    heap = sm.SymHeap(cfg, DEV)
+    idx = torch.from_numpy(idx_np.astype(np.int32)).to(DEV)
+    w = torch.from_numpy(w_np.astype(np.float32)).to(DEV)
+    out = torch.empty((n, cfg["hidden"]), dtype=torch.bfloat16, device=DEV)
+    if fused:
+        # the fused launch routes from logits itself: feed logits that select idx
+        lg = torch.full((n, cfg["num_experts"]), -30.0, dtype=torch.float32)
+        for j in range(k):
+            lg[torch.arange(n), torch.from_numpy(idx_np[:, j]).long()] = 10.0 - j * 1e-3
+        idx_out = torch.empty_like(idx)
+        w_out = torch.empty_like(w)
+        heap.pipeline(lg.to(DEV), x, wg, wu, wd, idx_out, w_out, out, fused=1)
+        torch.cuda.synchronize()
+        assert torch.equal(idx_out, idx)
+        return heap, out, w_out.cpu().numpy()
+    heap.dispatch(x, idx, w)
+    heap.expert_ffn(wg, wu, wd)
+    heap.combine(idx, w, out)
+    torch.cuda.synchronize()
+    return heap, out, w_np
+
+
+@pytest.mark.parametrize("fused", [0, 1])
+def test_all_pairs_on_two_experts(sm, fused):
+    cfg = dict(world=4, tokens_per_slot=150, hidden=256, num_experts=8, topk=2, inter=256)
+    n = 600
+    idx = np.tile(np.array([[0, 1]]), (n, 1))
+    idx[::2] = [1, 0]                                  # order within a token varies
+    w = np.tile(np.array([[0.75, 0.25]], dtype=np.float32), (n, 1))
+    heap, out, w_used = _run(sm, cfg, idx, w, fused)
+    assert heap.status() == 0
+    ref = _oracle_from_idx(cfg, idx, w_used, fresh_weight_fn(cfg, DEV))
+    assert ref["cnt"].tolist() == [600, 600, 0, 0, 0, 0, 0, 0]
+    assert np.array_equal(heap.pos(0).cpu().numpy(), ref["pos"][:150])
+    assert_close(bits(out), bf16_f64(ref["out"]), "two-expert out")
+
+
+@pytest.mark.parametrize("fused", [0, 1])
+def test_max_experts_and_topk(sm, fused):
+    cfg = dict(world=8, tokens_per_slot=40, hidden=128, num_experts=1024, topk=32, inter=128)
+    n, k = 320, 32
+    lg = ms.logits_np(cfg)
+    idx, w = oracle.route_topk(lg, k)
+    heap, out, w_used = _run(sm, cfg, idx, w, fused)
+    assert heap.status() == 0
+    ref = _oracle_from_idx(cfg, idx, w_used, fresh_weight_fn(cfg, DEV))
+    assert_close(bits(out), bf16_f64(ref["out"]), "E=1024 k=32 out")
+
+
+@pytest.mark.parametrize("fused", [0, 1])
+def test_single_expert_ragged_tokens(sm, fused):
+    cfg = dict(world=1, tokens_per_slot=333, hidden=384, num_experts=1, topk=1, inter=384)
+    n = 333
+    idx = np.zeros((n, 1), dtype=np.int64)
+    w = np.ones((n, 1), dtype=np.float32)
+    heap, out, w_used = _run(sm, cfg, idx, w, fused)
+    assert heap.status() == 0
+    ref = _oracle_from_idx(cfg, idx, w_used, fresh_weight_fn(cfg, DEV))
+    t = int(ref["tot"][0])
+    assert_close(bits(heap.y(0)[:t]), ref["y_exact"][0], "single expert y")
+    assert_close(bits(out), bf16_f64(ref["out"]), "single expert out")
+
+
+def test_ragged_world_and_tokens_through_pipeline(sm):
+    cfg = dict(world=3, tokens_per_slot=100, hidden=256, num_experts=6, topk=2, inter=128)
+    logits, x, wg, wu, wd = device_inputs(cfg, DEV)
+    n = 300
+    heap = sm.SymHeap(cfg, DEV)
+    outs = []
+    for fused in (0, 1, 0):
+        idx = torch.empty((n, 2), dtype=torch.int32, device=DEV)
+        w = torch.empty((n, 2), dtype=torch.float32, device=DEV)
+        out = torch.empty((n, cfg["hidden"]), dtype=torch.bfloat16, device=DEV)
+        heap.pipeline(logits, x, wg, wu, wd, idx, w, out, fused=fused)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert heap.status() == 0
+    assert all(torch.equal(o.view(torch.int16), outs[0].view(torch.int16)) for o in outs)
+    ref = oracle.pipeline(ms.logits_np(cfg), ms.x_np(cfg), cfg, fresh_weight_fn(cfg, DEV))
+    assert_close(bits(outs[0]), bf16_f64(ref["out"]), "W=3 T=100 out")
