@@ -8,7 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/symmoe.h"
+#include "symmoe.h"  // include/ (on the include path)
 
 namespace symmoe {
 
