@@ -39,12 +39,30 @@ constexpr int UK = 16;
 constexpr int BN = 256;         // tokens per pair tile (tcgen05 N)
 constexpr int STAGES = 6;
 constexpr int A_BYTES = 128 * BK * 2;          // 16 KB: this CTA's weight rows
-constexpr int B_ROWS = BN / 2;                 // this CTA's token rows (TMA box)
+constexpr int B_ROWS = BN / 2;                 // this CTA's token rows at most (largest box)
 constexpr int B_BYTES = B_ROWS * BK * 2;       // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES; // 32 KB
 constexpr int ACC_COLS = BN;
 constexpr int TMEM_COLS = 512;
 constexpr int XCH_BYTES = 2 * 2 * 2 * 16 * 32 * 4;  // pairs x buffers x directions x 16 cols x 32 lanes
+
+// Token-row boxes: a tile loads only the token rows its MMA reads (N/2 per
+// CTA, a multiple of 8), rounded up to the next of 8, 16, ..., 128 rows, so a
+// ragged tile of a few rows does not stream 128 rows of B per K block.
+constexpr int NBOX = 5;
+constexpr int BOX_MIN_ROWS = 8;
+struct BMaps {
+  CUtensorMap m[NBOX];  // m[i]: box of BOX_MIN_ROWS << i rows
+};
+__host__ __device__ inline int box_index(int half_rows) {
+  int i = 0;
+  while (i < NBOX - 1 && (BOX_MIN_ROWS << i) < half_rows) ++i;
+  return i;
+}
+// bytes both CTAs' copies of one K block deliver to the leader's full barrier
+__host__ __device__ inline uint32_t stage_tx(int box) {
+  return 2u * (uint32_t)(A_BYTES + (BOX_MIN_ROWS << box) * BK * 2);
+}
 
 enum Kind : int { GATE_UP = 0, DOWN = 1 };
 
@@ -117,6 +135,104 @@ __device__ inline TileInfo decode(const sym_heap &h, const Tables &tb, int t) {
 }
 
 __device__ __forceinline__ int n_mma(int valid) { return min(BN, (valid + 15) & ~15); }
+
+// Tables shared by both GEMM kinds (the fused pipeline runs both in one
+// launch): token tiles of BN rows per expert, tokprefix = exclusive prefix of
+// token tiles.  Kind k enumerates, per expert, f-major then token tile, so
+// its tile prefix is tokprefix * nf_k.
+struct TokTables {
+  int *cnt, *roff, *tokprefix;
+};
+__host__ __device__ constexpr size_t tok_tables_bytes(int num_experts) {
+  return (size_t)(3 * num_experts + 1) * sizeof(int);
+}
+__device__ inline void build_tok_tables(const sym_heap &h, const TokTables &tb) {
+  const int E = h.s.num_experts, E_loc = E / h.s.world;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int d = e / E_loc, l = e % E_loc;
+    tb.cnt[e] = __ldcg(win<const int32_t>(h, d, h.off_cnt) + l);
+    tb.roff[e] = __ldcg(win<const int32_t>(h, d, h.off_recv_off) + l);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    if (lane == 0) tb.tokprefix[0] = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int v = e < E ? (tb.cnt[e] + BN - 1) / BN : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (e < E) tb.tokprefix[e + 1] = carry + incl;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+}
+__device__ inline TileInfo decode_tok(const sym_heap &h, const TokTables &tb, int nf, int t) {
+  const int E = h.s.num_experts;
+  const int key = t / nf;  // expert e owns tiles [tokprefix[e]*nf, tokprefix[e+1]*nf)
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tb.tokprefix[mid] <= key) lo = mid; else hi = mid;
+  }
+  TileInfo ti;
+  ti.e = lo;
+  const int c = tb.cnt[lo];
+  const int ntok = (c + BN - 1) / BN;
+  const int local = t - tb.tokprefix[lo] * nf;
+  ti.f = local / ntok;
+  ti.n = local % ntok;
+  ti.d = lo / (E / h.s.world);
+  ti.row0 = tb.roff[lo] + ti.n * BN;
+  ti.valid = min(BN, c - ti.n * BN);
+  return ti;
+}
+
+// Bounded mbarrier wait that also gives up once *stop <= t (the producer
+// stopped before tile t) or *abort is set; a timeout sets *abort and the
+// heap's SYM_STATUS_TIMEOUT bit.
+__device__ __forceinline__ bool wait_or_stop(uint64_t *bar, uint32_t parity, int t,
+                                             const volatile int *stop, volatile int *abort,
+                                             uint32_t timeout_us, const sym_heap &h) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = (uint64_t)timeout_us * 1000ull;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (*abort || *stop <= t) return false;
+    if ((it & 15u) == 15u && globaltimer_ns() - t0 > limit) {
+      *abort = 1;
+      raise_status(h, SYM_STATUS_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// The gate/up epilogue hands half of each 32-column chunk to its partner warp
+// (warps 2+pair and 4+pair: 64 threads on named barrier 1 + pair).
+__device__ __forceinline__ void xch_barrier(int pair) {
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
+}
+// The same barrier with an AND over `ok` of all 64 threads: both partner warps
+// take the same decision, so neither is left waiting on the other.
+__device__ __forceinline__ bool xch_vote(int pair, bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, 64, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "r"(1 + pair)
+      : "memory");
+  return r != 0;
+}
 
 // ---------------------------------------------------------------------------
 // cluster helpers
@@ -203,4 +319,16 @@ __device__ __forceinline__ void commit2_both(uint64_t *bar) {
 }
 
 }  // namespace gemm2
+
+// Tensor-map encoders (expert_ffn.cu): a bf16 matrix [rows][cols] with a box
+// of [box_rows][64]; a per-slot heap window [W][cap][cols] with the slot
+// stride as the outer stride.  Both use the 128-byte swizzle.
+bool encode_2d(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+bool encode_heap_3d(CUtensorMap *m, const sym_heap &h, uint64_t off, uint64_t cols,
+                    uint32_t box_rows);
+// the NBOX token-row maps of one heap window
+bool encode_heap_boxes(gemm2::BMaps *m, const sym_heap &h, uint64_t off, uint64_t cols);
+// Largest number of CTA pairs of `kern` (192 or 256 threads, `smem` bytes)
+// that can be resident at once (cached per device and kernel).
+int max_resident_pairs(const void *kern, int threads, size_t smem, int num_sms);
 }  // namespace symmoe
