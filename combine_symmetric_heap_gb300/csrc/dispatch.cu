@@ -10,7 +10,8 @@
 // ascending inside a slot; inside one expert by (source slot, token, k),
 // i.e. by global token g because the k experts of a token are distinct.
 //
-// Three launches:
+// Three launches (scan and scatter with programmatic dependent launch: each is
+// scheduled while its predecessor drains and waits for its results on the device):
 //   count   one CTA per 128-token chunk: per-expert bitmask of the chunk's
 //           tokens in shared memory -> each pair's rank inside the chunk
 //           (popcount of the lower bits) and the chunk histogram.
@@ -35,6 +36,7 @@ __global__ void __launch_bounds__(CHUNK) dispatch_count_kernel(sym_heap h,
   const int chunk = blockIdx.x;
   const int t = threadIdx.x;
   const int g = chunk * CHUNK + t;
+  pdl_launch_dependents();  // the scan may be scheduled now; it waits for this grid
   for (int i = t; i < E * (CHUNK / 32); i += CHUNK) mask[i] = 0;
   __syncthreads();
   const uint32_t bit = 1u << (t & 31);
@@ -82,6 +84,8 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(sym_heap h) {
   const int nchunks = (N + CHUNK - 1) / CHUNK;
   int32_t *hist = win<int32_t>(h, 0, h.off_hist);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  pdl_launch_dependents();
+  pdl_wait();  // the count kernel's histogram
   // per expert: exclusive scan over chunks (warp scan, 32 chunks at a time)
   for (int e = wid; e < E; e += nw) {
     int32_t *row = hist + (size_t)e * nchunks;
@@ -129,6 +133,7 @@ __global__ void __launch_bounds__(SCATTER_THREADS)
   const int tid = threadIdx.x;
   const int nvec = H / 8;  // 16-byte vectors per row
   const uint4 *src = x + (size_t)g * nvec;
+  pdl_wait();  // offsets from the scan; nothing is touched before it
 
   // start the row loads before resolving the destinations
   uint4 v[SCATTER_VEC_PER_THREAD];
@@ -180,10 +185,13 @@ __global__ void __launch_bounds__(SCATTER_THREADS)
     win<int32_t>(h, d, h.off_recv_pair)[p] = g * k + tid;
     win<float>(h, d, h.off_recv_w)[p] = w[(size_t)g * k + tid];
   }
-  __threadfence();
+  // every thread's stores precede the barrier; the fence of each signalling
+  // thread is cumulative over them (release of the row block)
   __syncthreads();
-  if (tid < k && row_s[tid] >= 0)
+  if (tid < k && row_s[tid] >= 0) {
+    __threadfence();
     atomicAdd(win<uint32_t>(h, slot_s[tid], h.off_ready) + row_s[tid] / SYM_ROWS_PER_FLAG, 1u);
+  }
 }
 
 cudaError_t launch_dispatch(const sym_heap &h, const uint16_t *x, const int32_t *idx,
@@ -192,10 +200,13 @@ cudaError_t launch_dispatch(const sym_heap &h, const uint16_t *x, const int32_t 
   const int nchunks = (N + CHUNK - 1) / CHUNK;
   const size_t mask_bytes = (size_t)h.s.num_experts * (CHUNK / 32) * sizeof(uint32_t);
   dispatch_count_kernel<<<nchunks, CHUNK, mask_bytes, st>>>(h, idx);
-  dispatch_scan_kernel<<<1, 1024, 0, st>>>(h);
-  dispatch_scatter_kernel<<<N, SCATTER_THREADS, 0, st>>>(h, reinterpret_cast<const uint4 *>(x),
-                                                          idx, w);
-  return cudaGetLastError();
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  // scan and scatter are scheduled while their predecessor drains (they wait
+  // for its results on the device)
+  if ((err = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(1024), 0, st, h)) != cudaSuccess) return err;
+  return launch_pdl(dispatch_scatter_kernel, dim3(N), dim3(SCATTER_THREADS), 0, st, h,
+                    reinterpret_cast<const uint4 *>(x), idx, w);
 }
 
 }  // namespace symmoe

@@ -19,7 +19,7 @@
 //            the tcgen05.mma; two accumulator buffers let the epilogue of
 //            tile i overlap the main loop of tile i+1;
 //   warps 2-5 epilogue: tcgen05.ld, SwiGLU / bf16 rounding, stores.
-// Pair tiles are taken round-robin; row counts come from the dispatch signal
+// Pair tiles follow a rotated static schedule (pair_tile); row counts come from the dispatch signal
 // area on the device (no host sync).
 #include <mutex>
 
@@ -36,7 +36,7 @@ constexpr int G2_CTRL_BYTES = 256;
 
 static size_t gemm2_smem_bytes(int num_experts) {
   return 1024 + (size_t)gemm2::STAGES * gemm2::STAGE_BYTES + gemm2::XCH_BYTES + G2_CTRL_BYTES +
-         gemm2::tables_bytes(num_experts);
+         gemm2::tok_tables_bytes(num_experts);
 }
 
 template <int KIND>
@@ -48,31 +48,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *ring = smem;
-  float *xch = reinterpret_cast<float *>(smem + (size_t)STAGES * STAGE_BYTES);
   uint8_t *ctrl = smem + (size_t)STAGES * STAGE_BYTES + XCH_BYTES;
-  uint64_t *full = reinterpret_cast<uint64_t *>(ctrl);
-  uint64_t *empty = full + STAGES;
-  uint64_t *acc_full = empty + STAGES;
-  uint64_t *acc_empty = acc_full + 2;
-  uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(acc_empty + 2);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(ctrl);  // full[6] empty[6] acc_full[2] acc_empty[2] acc_head[2]
+  uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 6);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base_s + 1);
   volatile int *stop_tile = abort_flag + 1;
   const int E = h.s.num_experts;
   int *tab = reinterpret_cast<int *>(ctrl + G2_CTRL_BYTES);
-  const Tables tb{tab, tab + E, tab + 2 * E};
+  const TokTables tb{tab, tab + E, tab + 2 * E};
   const int wid = warp_id(), lane = lane_id();
-  const uint32_t rank = cta_rank();
   const int pair_id = (int)cluster_id_x(), npairs = (int)num_clusters_x();
+  Pipe p;
+  p.ring = smem;
+  p.xch = reinterpret_cast<float *>(smem + (size_t)STAGES * STAGE_BYTES);
+  p.full = bars;
+  p.empty = bars + STAGES;
+  p.acc_full = bars + 2 * STAGES;
+  p.acc_empty = bars + 2 * STAGES + 2;
+  p.acc_head = bars + 2 * STAGES + 4;
+  p.rank = cta_rank();
+  p.abort = abort_flag;
+  p.stop = stop_tile;
+  p.tmo = h.wait_timeout_us;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);  // used on the leader: one arrive (with both CTAs' bytes)
-      mbar_init(&empty[s], 1);
+      mbar_init(&p.full[s], 1);  // used on the leader: one arrive (with both CTAs' bytes)
+      mbar_init(&p.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 8);  // leader: 4 epilogue warps of each CTA
+      mbar_init(&p.acc_full[b], 1);
+      mbar_init(&p.acc_empty[b], 8);  // leader: 4 epilogue warps of each CTA
+      mbar_init(&p.acc_head[b], 8);
     }
     *abort_flag = 0;
     *stop_tile = 0x7fffffff;
@@ -85,210 +92,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     tmem_alloc2(tmem_base_s, TMEM_COLS);
     tmem_relinquish2();
   }
-  build_tables(h, tb, KIND);
+  build_tok_tables(h, tb);
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // barriers of both CTAs initialised before any remote arrive
   tc_fence_after();
-  const uint32_t tmem_base = *tmem_base_s;
-  const int total_tiles = tb.prefix[E];
-  const int nk = nk_of(h, KIND);
+  p.tmem_base = *tmem_base_s;
+  const int nf = nf_of(h, KIND);
+  const int total_tiles = tb.tokprefix[E] * nf;
   const uint32_t tmo = h.wait_timeout_us;
-
-  // this CTA's token rows of tile ti: the MMA takes n_mma rows, half per CTA
-  auto my_rows = [&](const gemm2::TileInfo &ti, int &r0, int &cnt) {
-    const int half = n_mma(ti.valid) / 2;
-    r0 = ti.row0 + (int)rank * half;
-    cnt = max(0, min(half, ti.valid - (int)rank * half));
-  };
-  auto rows_ready = [&](const gemm2::TileInfo &ti, bool block) -> bool {
-    int r0, cnt;
-    my_rows(ti, r0, cnt);
-    if (cnt == 0) return true;
-    const int total = *win<const int32_t>(h, ti.d, h.off_total);
-    const uint32_t *ready = win<const uint32_t>(h, ti.d, h.off_ready);
-    for (int b = r0 / SYM_ROWS_PER_FLAG; b <= (r0 + cnt - 1) / SYM_ROWS_PER_FLAG; ++b) {
-      const uint32_t target = (uint32_t)min(SYM_ROWS_PER_FLAG, total - b * SYM_ROWS_PER_FLAG);
-      if (block) {
-        if (!wait_counter_geq(ready + b, target, tmo, abort_flag)) return false;
-      } else if (ld_acquire_u32(ready + b) < target) {
-        return false;
-      }
-    }
-    return true;
+  auto wait = [&](const uint32_t *c, uint32_t target) { return wait_counter_geq(c, target, tmo, abort_flag); };
+  // the token rows of tile t dispatched (both CTAs check the whole tile)
+  auto tile_ready = [&](int t, bool block) {
+    const TileInfo ti = decode_tok(h, tb, nf, t);
+    return rows_ready(h, ti.d, ti.row0, ti.valid, block, wait);
   };
 
   if (wid == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      int stage = 0;
-      uint32_t phase = 0;
-      int t = pair_id;
-      const uint32_t full_leader = map_to(&full[0], 0);
+      ProdState ps;
+      int i = 0, t = pair_tile(0, pair_id, npairs);
       bool ready_ok = true;
       if (wait_ready && t < total_tiles) {
-        ready_ok = rows_ready(gemm2::decode(h, tb, t), true);
+        ready_ok = tile_ready(t, true);
         if (!ready_ok) {
           raise_status(h, SYM_STATUS_TIMEOUT);
           *stop_tile = t;
         }
       }
       while (ready_ok && t < total_tiles && !*abort_flag) {
-        if (wait_ready) fence_proxy_async();
-        const gemm2::TileInfo ti = gemm2::decode(h, tb, t);
-        int r0, cnt;
-        my_rows(ti, r0, cnt);
-        const int box = box_index(n_mma(ti.valid) / 2);
-        const uint32_t tx = stage_tx(box);
-        const int arow = KIND == GATE_UP ? ti.e * h.s.inter + ti.f * 128 + (int)rank * 64
-                                         : ti.e * h.s.hidden + ti.f * 256 + (int)rank * 128;
-        const int t_next = t + npairs;
+        if (wait_ready) fence_proxy_async();  // rows written by generic stores
+        const TileInfo ti = decode_tok(h, tb, nf, t);
+        const int t_next = pair_tile(i + 1, pair_id, npairs);
         bool next_ok = !wait_ready || t_next >= total_tiles;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!next_ok && kb == nk / 2) next_ok = rows_ready(gemm2::decode(h, tb, t_next), false);
-          if (!gemm2::wait_or_stop(&empty[stage], phase ^ 1u, -1, stop_tile, abort_flag, tmo, h)) break;
-          uint8_t *sb = ring + (size_t)stage * STAGE_BYTES;
-          const uint32_t bar = full_leader + (uint32_t)(stage * sizeof(uint64_t));
-          if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);  // both halves
-          if (KIND == GATE_UP) {
-            tma_load_2d_pair(sb, &tm_a0, bar, kb * BK, arow);               // 64 gate rows
-            tma_load_2d_pair(sb + A_BYTES / 2, &tm_a1, bar, kb * BK, arow);  // 64 up rows
-          } else {
-            tma_load_2d_pair(sb, &tm_a0, bar, kb * BK, arow);               // 128 down rows
-          }
-          tma_load_3d_pair(sb + A_BYTES, &tm_b.m[box], bar, kb * BK, r0, ti.d);  // this CTA's tokens
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!next_ok && !rows_ready(gemm2::decode(h, tb, t_next), true)) {
+        auto probe = [&]() {
+          if (!next_ok) next_ok = tile_ready(t_next, false);
+        };
+        if (!produce_tile<KIND>(h, p, ps, ti, &tm_a0, &tm_a1, tm_b, t, probe)) break;
+        if (!next_ok && !tile_ready(t_next, true)) {
           raise_status(h, SYM_STATUS_TIMEOUT);
           *stop_tile = t_next;
           break;
         }
         t = t_next;
+        ++i;
       }
     }
   } else if (wid == 1) {
-    if (lane == 0) {
-      int stage = 0, abuf = 0;
-      uint32_t phase = 0, aphase = 0;
-      if (rank == 0) {
-        // ---------------------------------------------------- MMA issuer (leader)
-        for (int t = pair_id; t < total_tiles; t += npairs) {
-          const gemm2::TileInfo ti = gemm2::decode(h, tb, t);
-          const uint32_t idesc = idesc_bf16_f32(256, n_mma(ti.valid));
-          if (!gemm2::wait_or_stop(&acc_empty[abuf], aphase ^ 1u, t, stop_tile, abort_flag, tmo, h)) break;
-          tc_fence_after();
-          const uint32_t d_tmem = tmem_base + (uint32_t)(abuf * ACC_COLS);
-          bool stopped = false;
-          for (int kb = 0; kb < nk; ++kb) {
-            if (!gemm2::wait_or_stop(&full[stage], phase, t, stop_tile, abort_flag, tmo, h)) {
-              stopped = true;
-              break;
-            }
-            tc_fence_after();
-            uint8_t *sb = ring + (size_t)stage * STAGE_BYTES;
-            const uint64_t da = smem_desc_sw128(sb), db = smem_desc_sw128(sb + A_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < BK / UK; ++kk) {
-              const uint64_t adv = (uint64_t)(kk * UK * 2 / 16);
-              mma2(d_tmem, da + adv, db + adv, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-            }
-            commit2_both(&empty[stage]);
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-          if (stopped) break;
-          commit2_both(&acc_full[abuf]);
-          if (++abuf == 2) {
-            abuf = 0;
-            aphase ^= 1u;
-          }
-        }
-      }
+    if (lane == 0 && p.rank == 0) {
+      // ---------------------------------------------------- MMA issuer (leader)
+      MmaState ms;
+      for (int i = 0, t; (t = pair_tile(i, pair_id, npairs)) < total_tiles; ++i)
+        if (!mma_tile<KIND>(h, p, ms, decode_tok(h, tb, nf, t), t)) break;
     }
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = wid & 3;  // TMEM lane quarter this warp may access
-    int abuf = 0;
-    uint32_t aphase = 0;
-    uint32_t chunk_ctr = 0;  // alternates the exchange buffers across all chunks
-    const uint32_t leader_acc_empty0 = map_to(&acc_empty[0], 0);
-    for (int t = pair_id; t < total_tiles; t += npairs) {
-      const gemm2::TileInfo ti = gemm2::decode(h, tb, t);
-      bool ok = gemm2::wait_or_stop(&acc_full[abuf], aphase, t, stop_tile, abort_flag, tmo, h);
-      // warp-collective TMEM loads and the gate/up exchange follow: decide together
-      ok = KIND == GATE_UP ? gemm2::xch_vote(q & 1, ok) : __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(abuf * ACC_COLS);
-      if (KIND == GATE_UP) {
-        const int pair = q & 1;  // gate lanes 32*pair.., up lanes 64 + 32*pair..
-        const bool is_gate = q < 2;
-        const int ld = h.s.inter;
-        const int feature = ti.f * 128 + (int)rank * 64 + pair * 32 + lane;
-        uint16_t *out = win<uint16_t>(h, ti.d, h.off_h) + (size_t)ti.row0 * ld + feature;
-        for (int c0 = 0; c0 < ti.valid; c0 += 32, ++chunk_ctr) {
-          uint32_t v[32];
-          tmem_ld32(tbase + c0, v);
-          tmem_ld_wait();
-          // xch[pair][buf][dir][16][32]: dir 0 carries up cols 0-15 to the
-          // gate warp, dir 1 carries gate cols 16-31 to the up warp
-          float *xb = xch + ((size_t)(pair * 2 + (chunk_ctr & 1)) * 2) * 16 * 32;
-          float *to_partner = xb + (is_gate ? 1 : 0) * 16 * 32;
-          const float *from_partner = xb + (is_gate ? 0 : 1) * 16 * 32;
-          // gate warps hand over columns 16-31, up warps columns 0-15
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            to_partner[c * 32 + lane] = __uint_as_float(is_gate ? v[16 + c] : v[c]);
-          gemm2::xch_barrier(pair);
-          const int keep = is_gate ? 0 : 16;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int col = c0 + keep + c;
-            const float other = from_partner[c * 32 + lane];
-            const float mine = __uint_as_float(is_gate ? v[c] : v[16 + c]);
-            const float gt = is_gate ? mine : other;
-            const float up = is_gate ? other : mine;
-            if (col < ti.valid) out[(size_t)col * ld] = to_bf16(gt / (1.0f + __expf(-gt)) * up);
-          }
-        }
-      } else {
-        const int ld = h.s.hidden;
-        const int feature = ti.f * 256 + (int)rank * 128 + q * 32 + lane;
-        uint16_t *out = win<uint16_t>(h, ti.d, h.off_y) + (size_t)ti.row0 * ld + feature;
-        const bool live = feature < ld;  // a last pair tile may run past H
-        for (int c0 = 0; c0 < ti.valid; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tbase + c0, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (live && c0 + c < ti.valid) out[(size_t)(c0 + c) * ld] = to_bf16(__uint_as_float(v[c]));
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (rank == 0) mbar_arrive(&acc_empty[abuf]);
-        else mbar_arrive_remote(leader_acc_empty0 + (uint32_t)(abuf * sizeof(uint64_t)));
-      }
-      if (++abuf == 2) {
-        abuf = 0;
-        aphase ^= 1u;
-      }
-    }
+    EpiState es;
+    for (int i = 0, t; (t = pair_tile(i, pair_id, npairs)) < total_tiles; ++i)
+      if (!epi_tile<KIND>(h, p, es, decode_tok(h, tb, nf, t), t, q, lane)) break;
   }
 
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // no remote arrive or MMA of the pair is still in flight
   tc_fence_after();
-  if (wid == 1) tmem_dealloc2(tmem_base, TMEM_COLS);
+  if (wid == 1) tmem_dealloc2(p.tmem_base, TMEM_COLS);
 }
 
 // ---------------------------------------------------------------------------

@@ -18,7 +18,7 @@
 //            counter of its 128-row block (release).
 //   phase 3  expert GEMM tiles on CTA pairs (the tcgen05 cta_group::2 tiles of
 //            the stand-alone GEMM): each pair takes its gate/up tiles, then its
-//            down tiles, round-robin.  A gate/up tile starts once the ready
+//            down tiles, in the rotated static schedule of the pair engine.  A gate/up tile starts once the ready
 //            counters of its token rows are complete; a down tile once every
 //            gate/up feature tile of its 256 token rows is stored (h_ready);
 //            each epilogue warp of both CTAs bumps h_ready / y_ready of the
@@ -299,7 +299,8 @@ __device__ inline void combine_token(const sym_heap &h, const FusedArgs &a, cons
     if (p >= 0) {
       // the 256-row down tile holding this row: every epilogue warp of every
       // feature tile has stored its share
-      ok = wait_geq(h, y_ready(h) + tb.tokprefix[e] + (p - tb.roff[e]) / gemm2::BN, target);
+      ok = wait_geq(h, y_ready(h) + tb.tokprefix[e] + gemm2::tile_of_row(tb.cnt[e], p - tb.roff[e]),
+                    target);
       src = win<const uint4>(h, e / E_loc, h.off_y) + (size_t)p * (H / 8);
     }
     src_s[lane] = src;
@@ -347,13 +348,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *ring = smem;
-  float *xch = reinterpret_cast<float *>(smem + (size_t)STAGES * STAGE_BYTES);
-  uint8_t *ctrl_s = smem + (size_t)STAGES * STAGE_BYTES + XCH_BYTES;
-  uint64_t *full = reinterpret_cast<uint64_t *>(ctrl_s);
-  uint64_t *empty = full + STAGES;
-  uint64_t *acc_full = empty + STAGES;
-  uint64_t *acc_empty = acc_full + 2;
-  uint64_t *drained = acc_empty + 2;  // every MMA of this launch has completed
+  uint8_t *xch_raw = smem + (size_t)STAGES * STAGE_BYTES;
+  uint8_t *ctrl_s = xch_raw + XCH_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(ctrl_s);  // full[6] empty[6] acc_full[2] acc_empty[2] acc_head[2]
+  uint64_t *drained = bars + 2 * STAGES + 6;  // every MMA of this launch has completed
   uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(drained + 1);
   volatile int *abort_s = reinterpret_cast<volatile int *>(tmem_base_s + 1);
   volatile int *never_s = abort_s + 1;  // "stop before tile" bound: never
@@ -362,24 +360,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
   int *tab = reinterpret_cast<int *>(ctrl_s + FUSED_CTRL_SMEM);
   const TokTables tb{tab, tab + E, tab + 2 * E};
   const int wid = warp_id(), lane = lane_id();
-  // per-warp destination / source pointer and weight tables (32 entries each)
-  uint8_t *warp_tab = ctrl_s + FUSED_CTRL_SMEM + ((tok_tables_bytes(E) + 15) & ~size_t(15));
-  void **ptr_s = reinterpret_cast<void **>(warp_tab) + wid * 32;
-  float *wgt_s = reinterpret_cast<float *>(warp_tab + FUSED_THREADS / 32 * 32 * sizeof(void *)) + wid * 32;
-  const uint32_t tmo = h.wait_timeout_us;
+  // per-warp destination / source pointer and weight tables of phases 2 and 4
+  // (32 entries each), in the exchange buffer, which only phase 3 uses
+  void **ptr_s = reinterpret_cast<void **>(xch_raw) + wid * 32;
+  float *wgt_s = reinterpret_cast<float *>(xch_raw + FUSED_THREADS / 32 * 32 * sizeof(void *)) + wid * 32;
   const int N = h.s.world * h.s.tokens_per_slot;
   const int nchunks = (N + FUSED_CHUNK - 1) / FUSED_CHUNK;
-  const uint32_t rank = cta_rank();
   const int pair_id = (int)cluster_id_x(), npairs = (int)num_clusters_x();
+  Pipe p;
+  p.ring = ring;
+  p.xch = reinterpret_cast<float *>(xch_raw);
+  p.full = bars;
+  p.empty = bars + STAGES;
+  p.acc_full = bars + 2 * STAGES;
+  p.acc_empty = bars + 2 * STAGES + 2;
+  p.acc_head = bars + 2 * STAGES + 4;
+  p.rank = cta_rank();
+  p.abort = abort_s;
+  p.stop = never_s;
+  p.tmo = h.wait_timeout_us;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);  // used on the leader: one arrive (with both CTAs' bytes)
-      mbar_init(&empty[s], 1);
+      mbar_init(&p.full[s], 1);  // used on the leader: one arrive (with both CTAs' bytes)
+      mbar_init(&p.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 8);  // leader: 4 epilogue warps of each CTA
+      mbar_init(&p.acc_full[b], 1);
+      mbar_init(&p.acc_empty[b], 8);  // leader: 4 epilogue warps of each CTA
+      mbar_init(&p.acc_head[b], 8);
     }
     mbar_init(drained, 1);
     *abort_s = 0;
@@ -401,7 +410,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
   __syncthreads();
   cluster_sync();  // barriers of both CTAs initialised before any remote arrive
   tc_fence_after();
-  const uint32_t tmem_base = *tmem_base_s;
+  p.tmem_base = *tmem_base_s;
 
   // ---------------- phase 1: route + count (the last finisher scans)
   for (;;) {
@@ -440,240 +449,89 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
     const int nf1 = nf_of(h, GATE_UP), nf2 = nf_of(h, DOWN);
     const int total1 = tb.tokprefix[E] * nf1, total2 = tb.tokprefix[E] * nf2;
     const uint32_t h_target = EPI_WARPS_PER_TILE * (uint32_t)nf1;
-    using GU = std::integral_constant<int, GATE_UP>;
-    using DN = std::integral_constant<int, DOWN>;
-    // this CTA's token rows of a tile: the MMA takes n_mma rows, half per CTA
-    auto my_rows = [&](const TileInfo &ti, int &r0, int &cnt) {
-      const int half = n_mma(ti.valid) / 2;
-      r0 = ti.row0 + (int)rank * half;
-      cnt = max(0, min(half, ti.valid - (int)rank * half));
-    };
-    // inputs of a tile in place: the dispatched rows (gate/up) or every
-    // gate/up feature tile of the token tile (down)
-    auto inputs_ready = [&](int kind, const TileInfo &ti, bool block) -> bool {
+    auto wait = [&](const uint32_t *c, uint32_t target) { return wait_geq(h, c, target); };
+    // inputs of a tile in place: its dispatched rows (gate/up) or every
+    // gate/up feature tile of its token tile (down)
+    auto inputs_ready = [&](int kind, int t, bool block) -> bool {
+      const TileInfo ti = decode_tok(h, tb, kind == GATE_UP ? nf1 : nf2, t);
       if (kind == DOWN) {
         const uint32_t *c = h_ready(h) + tb.tokprefix[ti.e] + ti.n;
         return block ? wait_geq(h, c, h_target) : ld_acquire_u32(c) >= h_target;
       }
-      int r0, cnt;
-      my_rows(ti, r0, cnt);
-      if (cnt == 0) return true;
-      const int total = __ldcg(win<const int32_t>(h, ti.d, h.off_total));
-      const uint32_t *ready = win<const uint32_t>(h, ti.d, h.off_ready);
-      for (int b = r0 / SYM_ROWS_PER_FLAG; b <= (r0 + cnt - 1) / SYM_ROWS_PER_FLAG; ++b) {
-        const uint32_t target = (uint32_t)min(SYM_ROWS_PER_FLAG, total - b * SYM_ROWS_PER_FLAG);
-        if (block ? !wait_geq(h, ready + b, target) : ld_acquire_u32(ready + b) < target) return false;
-      }
-      return true;
+      return rows_ready(h, ti.d, ti.row0, ti.valid, block, wait);
     };
-    // the pair's tile after (kind, t): its gate/up tiles, then its down tiles
-    auto next_of = [&](int &kind, int &t) {
-      t += npairs;
-      if (kind == GATE_UP && t >= total1) {
+    // the pair's tiles: its gate/up tiles, then its down tiles, each list in
+    // the rotated static schedule; (kind, i) = the pair's i-th tile of a list
+    auto tile_at = [&](int i) { return pair_tile(i, pair_id, npairs); };
+    auto valid_at = [&](int kind, int i) { return tile_at(i) < (kind == GATE_UP ? total1 : total2); };
+    auto next_of = [&](int &kind, int &i) {
+      ++i;
+      if (kind == GATE_UP && !valid_at(GATE_UP, i)) {
         kind = DOWN;
-        t = pair_id;
+        i = 0;
       }
     };
-    auto total_of = [&](int kind) { return kind == GATE_UP ? total1 : total2; };
-    auto nf_k = [&](int kind) { return kind == GATE_UP ? nf1 : nf2; };
+    int kind0 = GATE_UP;
+    if (!valid_at(GATE_UP, 0)) kind0 = DOWN;
 
     if (wid == 0) {
       if (lane == 0) {
         // ------------------------------------------------------------ producer
-        int stage = 0;
-        uint32_t phase = 0;
-        const uint32_t full_leader = map_to(&full[0], 0);
-        auto produce = [&](auto kd, const TileInfo &ti, int kind_n, int t_n, bool &next_ok) -> bool {
-          constexpr int KIND = decltype(kd)::value;
-          int r0, cnt;
-          my_rows(ti, r0, cnt);
-          const CUtensorMap *ma = KIND == GATE_UP ? &tm_g : &tm_d;
-          const int box = box_index(n_mma(ti.valid) / 2);
-          const uint32_t tx = stage_tx(box);
-          const CUtensorMap *mb = KIND == GATE_UP ? &tm_rx.m[box] : &tm_h.m[box];
-          const int arow = KIND == GATE_UP ? ti.e * h.s.inter + ti.f * 128 + (int)rank * 64
-                                           : ti.e * h.s.hidden + ti.f * 256 + (int)rank * 128;
-          const int nk = nk_of(h, KIND);
-          for (int kb = 0; kb < nk; ++kb) {
-            if (!next_ok && kb == nk / 2)
-              next_ok = inputs_ready(kind_n, decode_tok(h, tb, nf_k(kind_n), t_n), false);
-            if (!wait_or_stop(&empty[stage], phase ^ 1u, -1, never_s, abort_s, tmo, h)) return false;
-            uint8_t *sb = ring + (size_t)stage * STAGE_BYTES;
-            const uint32_t bar = full_leader + (uint32_t)(stage * sizeof(uint64_t));
-            if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);  // both halves
-            if (KIND == GATE_UP) {
-              tma_load_2d_pair(sb, ma, bar, kb * BK, arow);               // 64 gate rows
-              tma_load_2d_pair(sb + A_BYTES / 2, &tm_u, bar, kb * BK, arow);  // 64 up rows
-            } else {
-              tma_load_2d_pair(sb, ma, bar, kb * BK, arow);               // 128 down rows
-            }
-            tma_load_3d_pair(sb + A_BYTES, mb, bar, kb * BK, r0, ti.d);   // this CTA's tokens
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-          return true;
-        };
-        int kind = GATE_UP, t = pair_id;
-        if (t >= total1) {
-          kind = DOWN;
-          t = pair_id;
-        }
-        bool ok = t < total_of(kind) ? inputs_ready(kind, decode_tok(h, tb, nf_k(kind), t), true) : true;
-        while (ok && t < total_of(kind) && !*abort_s) {
+        ProdState ps;
+        int kind = kind0, i = 0;
+        bool ok = valid_at(kind, i) ? inputs_ready(kind, tile_at(i), true) : true;
+        while (ok && valid_at(kind, i) && !*abort_s) {
           fence_proxy_async();  // the inputs were written by generic stores in this launch
-          const TileInfo ti = decode_tok(h, tb, nf_k(kind), t);
-          int kind_n = kind, t_n = t;
-          next_of(kind_n, t_n);
-          const bool has_next = t_n < total_of(kind_n);
+          const int t = tile_at(i);
+          int kind_n = kind, i_n = i;
+          next_of(kind_n, i_n);
+          const bool has_next = valid_at(kind_n, i_n);
+          const int t_n = tile_at(i_n);
           bool next_ok = !has_next;
-          ok = kind == GATE_UP ? produce(GU{}, ti, kind_n, t_n, next_ok)
-                               : produce(DN{}, ti, kind_n, t_n, next_ok);
+          auto probe = [&]() {
+            if (!next_ok) next_ok = inputs_ready(kind_n, t_n, false);
+          };
+          ok = kind == GATE_UP
+                   ? produce_tile<GATE_UP>(h, p, ps, decode_tok(h, tb, nf1, t), &tm_g, &tm_u, tm_rx, -1, probe)
+                   : produce_tile<DOWN>(h, p, ps, decode_tok(h, tb, nf2, t), &tm_d, &tm_d, tm_h, -1, probe);
           if (!ok) break;
-          if (has_next && !next_ok) ok = inputs_ready(kind_n, decode_tok(h, tb, nf_k(kind_n), t_n), true);
+          if (has_next && !next_ok) ok = inputs_ready(kind_n, t_n, true);
           kind = kind_n;
-          t = t_n;
+          i = i_n;
         }
         if (!ok) *abort_s = 1;
       }
     } else if (wid == 1) {
-      if (lane == 0 && rank == 0) {
+      if (lane == 0 && p.rank == 0) {
         // ------------------------------------------------------ MMA issuer (leader)
-        int stage = 0, abuf = 0;
-        uint32_t phase = 0, aphase = 0;
-        auto mma_tile = [&](auto kd, const TileInfo &ti) -> bool {
-          constexpr int KIND = decltype(kd)::value;
-          const uint32_t idesc = idesc_bf16_f32(256, n_mma(ti.valid));
-          if (!wait_or_stop(&acc_empty[abuf], aphase ^ 1u, -1, never_s, abort_s, tmo, h)) return false;
-          tc_fence_after();
-          const uint32_t d_tmem = tmem_base + (uint32_t)(abuf * ACC_COLS);
-          const int nk = nk_of(h, KIND);
-          for (int kb = 0; kb < nk; ++kb) {
-            if (!wait_or_stop(&full[stage], phase, -1, never_s, abort_s, tmo, h)) return false;
-            tc_fence_after();
-            uint8_t *sb = ring + (size_t)stage * STAGE_BYTES;
-            const uint64_t da = smem_desc_sw128(sb), db = smem_desc_sw128(sb + A_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < BK / UK; ++kk) {
-              const uint64_t adv = (uint64_t)(kk * UK * 2 / 16);
-              mma2(d_tmem, da + adv, db + adv, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-            }
-            commit2_both(&empty[stage]);
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-          commit2_both(&acc_full[abuf]);
-          if (++abuf == 2) {
-            abuf = 0;
-            aphase ^= 1u;
-          }
-          return true;
-        };
-        for (int kind = GATE_UP, t = pair_id; kind <= DOWN;) {
-          if (t >= total_of(kind)) {
-            if (kind == DOWN) break;
-            kind = DOWN;
-            t = pair_id;
-            continue;
-          }
-          const TileInfo ti = decode_tok(h, tb, nf_k(kind), t);
-          if (!(kind == GATE_UP ? mma_tile(GU{}, ti) : mma_tile(DN{}, ti))) break;
-          t += npairs;
+        MmaState ms;
+        for (int kind = kind0, i = 0; valid_at(kind, i); next_of(kind, i)) {
+          const int t = tile_at(i);
+          const bool ok = kind == GATE_UP ? mma_tile<GATE_UP>(h, p, ms, decode_tok(h, tb, nf1, t), -1)
+                                          : mma_tile<DOWN>(h, p, ms, decode_tok(h, tb, nf2, t), -1);
+          if (!ok) break;
         }
         // after an abort the epilogue may stop before the last accumulator:
         // wait for the MMAs still in flight before TMEM is released
         commit2_both(drained);
-        mbar_wait(drained, 0, tmo, nullptr);
+        mbar_wait(drained, 0, p.tmo, nullptr);
       }
     } else if (wid < 6) {
       // -------------------------------------------------------------- epilogue
       const int q = wid & 3;  // TMEM lane quarter this warp may access
-      int abuf = 0;
-      uint32_t aphase = 0;
-      uint32_t chunk_ctr = 0;
-      const uint32_t leader_acc_empty0 = map_to(&acc_empty[0], 0);
-      auto epi_tile = [&](auto kd, const TileInfo &ti) -> bool {
-        constexpr int KIND = decltype(kd)::value;
-        bool ok = wait_or_stop(&acc_full[abuf], aphase, -1, never_s, abort_s, tmo, h);
-        // warp-collective TMEM loads and the gate/up exchange follow: decide together
-        ok = KIND == GATE_UP ? xch_vote(q & 1, ok) : __all_sync(0xffffffffu, ok);
-        if (!ok) return false;
-        tc_fence_after();
-        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(abuf * ACC_COLS);
-        if (KIND == GATE_UP) {
-          const int pair = q & 1;  // gate lanes 32*pair.., up lanes 64 + 32*pair..
-          const bool is_gate = q < 2;
-          const int ld = h.s.inter;
-          const int feature = ti.f * 128 + (int)rank * 64 + pair * 32 + lane;
-          uint16_t *out = win<uint16_t>(h, ti.d, h.off_h) + (size_t)ti.row0 * ld + feature;
-          for (int c0 = 0; c0 < ti.valid; c0 += 32, ++chunk_ctr) {
-            uint32_t v[32];
-            tmem_ld32(tbase + c0, v);
-            tmem_ld_wait();
-            float *xb = xch + ((size_t)(pair * 2 + (chunk_ctr & 1)) * 2) * 16 * 32;
-            float *to_partner = xb + (is_gate ? 1 : 0) * 16 * 32;
-            const float *from_partner = xb + (is_gate ? 0 : 1) * 16 * 32;
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-              to_partner[c * 32 + lane] = __uint_as_float(is_gate ? v[16 + c] : v[c]);
-            xch_barrier(pair);
-            const int keep = is_gate ? 0 : 16;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int col = c0 + keep + c;
-              const float other = from_partner[c * 32 + lane];
-              const float mine = __uint_as_float(is_gate ? v[c] : v[16 + c]);
-              const float gt = is_gate ? mine : other;
-              const float up = is_gate ? other : mine;
-              if (col < ti.valid) out[(size_t)col * ld] = to_bf16(gt / (1.0f + __expf(-gt)) * up);
-            }
-          }
-        } else {
-          const int ld = h.s.hidden;
-          const int feature = ti.f * 256 + (int)rank * 128 + q * 32 + lane;
-          uint16_t *out = win<uint16_t>(h, ti.d, h.off_y) + (size_t)ti.row0 * ld + feature;
-          const bool live = feature < ld;
-          for (int c0 = 0; c0 < ti.valid; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tbase + c0, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (live && c0 + c < ti.valid) out[(size_t)(c0 + c) * ld] = to_bf16(__uint_as_float(v[c]));
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if (rank == 0) mbar_arrive(&acc_empty[abuf]);
-          else mbar_arrive_remote(leader_acc_empty0 + (uint32_t)(abuf * sizeof(uint64_t)));
-        }
-        if (++abuf == 2) {
-          abuf = 0;
-          aphase ^= 1u;
-        }
+      EpiState es;
+      for (int kind = kind0, i = 0; valid_at(kind, i); next_of(kind, i)) {
+        const TileInfo ti = decode_tok(h, tb, kind == GATE_UP ? nf1 : nf2, tile_at(i));
+        const bool ok = kind == GATE_UP ? epi_tile<GATE_UP>(h, p, es, ti, -1, q, lane)
+                                        : epi_tile<DOWN>(h, p, es, ti, -1, q, lane);
+        if (!ok) break;
         // publish this warp's share of the tile (read next by TMA or by the
         // combine's generic loads in other CTAs)
         __threadfence();
         asm volatile("fence.proxy.async.global;" ::: "memory");
         __syncwarp();
         if (lane == 0)
-          atomicAdd((KIND == GATE_UP ? h_ready(h) : y_ready(h)) + tb.tokprefix[ti.e] + ti.n, 1u);
-        return true;
-      };
-      for (int kind = GATE_UP, t = pair_id; kind <= DOWN;) {
-        if (t >= total_of(kind)) {
-          if (kind == DOWN) break;
-          kind = DOWN;
-          t = pair_id;
-          continue;
-        }
-        const TileInfo ti = decode_tok(h, tb, nf_k(kind), t);
-        if (!(kind == GATE_UP ? epi_tile(GU{}, ti) : epi_tile(DN{}, ti))) break;
-        t += npairs;
+          atomicAdd((kind == GATE_UP ? h_ready(h) : y_ready(h)) + tb.tokprefix[ti.e] + ti.n, 1u);
       }
     }
     if (*abort_s) set_abort(h);
@@ -700,7 +558,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
   __syncthreads();
   cluster_sync();  // no remote arrive or MMA of the pair is still in flight
   tc_fence_after();
-  if (wid == 1) tmem_dealloc2(tmem_base, TMEM_COLS);
+  if (wid == 1) tmem_dealloc2(p.tmem_base, TMEM_COLS);
   if (threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(ctl(h) + C_EXIT, 1u) == gridDim.x - 1) {
@@ -732,9 +590,10 @@ cudaError_t launch_fused(const sym_heap &h, const float *logits, const uint16_t 
       !encode_heap_boxes(&trx, h, h.off_recv_x, H) ||
       !encode_2d(&td, wd, (uint64_t)E * H, I, 128) || !encode_heap_boxes(&th, h, h.off_h, I))
     return cudaErrorInvalidValue;
+  static_assert(FUSED_THREADS / 32 * 32 * (sizeof(void *) + sizeof(float)) <= (size_t)XCH_BYTES,
+                "per-warp tables live in the exchange buffer");
   const size_t smem = 1024 + (size_t)STAGES * STAGE_BYTES + XCH_BYTES + FUSED_CTRL_SMEM +
-                      ((tok_tables_bytes(E) + 15) & ~size_t(15)) +
-                      FUSED_THREADS / 32 * 32 * (sizeof(void *) + sizeof(float));
+                      tok_tables_bytes(E);
   cudaError_t err = cudaFuncSetAttribute(moe_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
   if (err != cudaSuccess) return err;

@@ -1,13 +1,13 @@
-// gemm2sm.cuh -- the stand-alone expert GEMMs on CTA pairs (tcgen05
-// cta_group::2): one M=256 MMA spans the tensor cores of two SMs of a cluster.
+// gemm2sm.cuh -- the expert GEMM tiles on CTA pairs (tcgen05 cta_group::2):
+// one M=256 MMA spans the tensor cores of two SMs of a cluster.  Used by the
+// staged expert FFN and by the fused pipeline.
 //
 // Each CTA of the pair stages only its half of both operands: 128 of the 256
 // weight rows (A) and N/2 of the N token rows (B); the MMA, issued by the
 // pair's first CTA (the leader), reads the four halves from both shared
 // memories and leaves output rows 0-127 in the leader's TMEM and rows 128-255
 // in the peer's.  Per SM that is 32 KB of operands per 128 x 256 x 64
-// multiply-adds instead of 48 KB, so six stages fit and the ring keeps the
-// tensor pipe fed.
+// multiply-adds, so six stages fit and the ring keeps the tensor pipe fed.
 //
 //   GATE_UP: the pair computes 128 features x N tokens.  CTA r's A rows are
 //            the gate rows and the up rows of features f*128 + r*64 .. +63, so
@@ -18,6 +18,10 @@
 //   DOWN:    the pair computes 256 features x N tokens: CTA r holds the down
 //            rows f*256 + r*128 .. +127; y is written straight into the
 //            combine-in window.
+//
+// Token tiles hold BN = 256 rows; an expert with 257..288 rows has one tile
+// that carries the remainder through a second, narrow MMA on the same weight
+// stream, so it streams its weights once.
 //
 // Completion: the copies of both CTAs count their bytes on the leader's full
 // barrier (the .cta_group::2 form of the TMA copy), whose expected byte count
@@ -37,14 +41,16 @@ namespace gemm2 {
 constexpr int BK = 64;
 constexpr int UK = 16;
 constexpr int BN = 256;         // tokens per pair tile (tcgen05 N)
+constexpr int REM_MAX = 32;     // rows an expert's last tile may carry beyond BN (second MMA)
 constexpr int STAGES = 6;
 constexpr int A_BYTES = 128 * BK * 2;          // 16 KB: this CTA's weight rows
 constexpr int B_ROWS = BN / 2;                 // this CTA's token rows at most (largest box)
 constexpr int B_BYTES = B_ROWS * BK * 2;       // 16 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES; // 32 KB
+constexpr int B1_BYTES = REM_MAX / 2 * BK * 2; // 2 KB: this CTA's remainder rows
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + B1_BYTES;  // 34 KB
 constexpr int ACC_COLS = BN;
 constexpr int TMEM_COLS = 512;
-constexpr int XCH_BYTES = 2 * 2 * 2 * 16 * 32 * 4;  // pairs x buffers x directions x 16 cols x 32 lanes
+constexpr int XCH_BYTES = 2 * 2 * 16 * 32 * 4;  // pairs x directions x 16 cols x 32 lanes
 
 // Token-row boxes: a tile loads only the token rows its MMA reads (N/2 per
 // CTA, a multiple of 8), rounded up to the next of 8, 16, ..., 128 rows, so a
@@ -59,11 +65,6 @@ __host__ __device__ inline int box_index(int half_rows) {
   while (i < NBOX - 1 && (BOX_MIN_ROWS << i) < half_rows) ++i;
   return i;
 }
-// bytes both CTAs' copies of one K block deliver to the leader's full barrier
-__host__ __device__ inline uint32_t stage_tx(int box) {
-  return 2u * (uint32_t)(A_BYTES + (BOX_MIN_ROWS << box) * BK * 2);
-}
-
 enum Kind : int { GATE_UP = 0, DOWN = 1 };
 
 // features per pair tile and K blocks per kind
@@ -77,75 +78,46 @@ __host__ __device__ inline int nk_of(const sym_heap &h, int kind) {
 }
 
 struct TileInfo {
-  int e, f, n, d, row0, valid;
+  int e, f, n, d, row0, valid;  // valid: token rows of the tile, up to BN + REM_MAX
 };
 
-struct Tables {
-  int *cnt, *roff, *prefix;
+// Token tiles of an expert with c rows: BN rows each.  An expert with one
+// full tile and a remainder of at most REM_MAX rows (BN < c <= BN + REM_MAX)
+// streams its weights once: the remainder rides on that tile as a second MMA.
+// Such an expert is bound by its weight stream; with more full tiles the
+// expert is compute-bound, the narrow second MMA costs more than a separate
+// short tile, and the remainder gets a tile of its own.
+__host__ __device__ inline int ntok_of(int c) {
+  const int full = c / BN, rem = c % BN;
+  return full + ((rem > 0 && !(full == 1 && rem <= REM_MAX)) ? 1 : 0);
+}
+// the token tile of an expert holding its row r (0 <= r < c)
+__host__ __device__ inline int tile_of_row(int c, int r) { return min(r / BN, ntok_of(c) - 1); }
+
+// MMA widths of a tile: n0 for its first BN rows, n1 (0: none) for the rest;
+// each a multiple of 16 (rows past `valid` are computed and dropped)
+struct TileGeom {
+  int n0, n1;
 };
-__host__ __device__ constexpr size_t tables_bytes(int num_experts) {
-  return (size_t)(3 * num_experts + 1) * sizeof(int);
+__device__ __forceinline__ TileGeom geom(int valid) {
+  TileGeom g;
+  g.n0 = min(BN, (valid + 15) & ~15);
+  g.n1 = valid > BN ? ((valid - BN + 15) & ~15) : 0;
+  return g;
 }
 
-__device__ inline void build_tables(const sym_heap &h, const Tables &tb, int kind) {
-  const int E = h.s.num_experts, E_loc = E / h.s.world;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int d = e / E_loc, l = e % E_loc;
-    tb.cnt[e] = win<const int32_t>(h, d, h.off_cnt)[l];
-    tb.roff[e] = win<const int32_t>(h, d, h.off_recv_off)[l];
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x, nf = nf_of(h, kind);
-    int carry = 0;
-    if (lane == 0) tb.prefix[0] = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      const int e = e0 + lane;
-      const int v = e < E ? ((tb.cnt[e] + BN - 1) / BN) * nf : 0;
-      int incl = v;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-      }
-      if (e < E) tb.prefix[e + 1] = carry + incl;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-  }
-}
-
-__device__ inline TileInfo decode(const sym_heap &h, const Tables &tb, int t) {
-  const int E = h.s.num_experts;
-  int lo = 0, hi = E;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (tb.prefix[mid] <= t) lo = mid; else hi = mid;
-  }
-  TileInfo ti;
-  ti.e = lo;
-  const int c = tb.cnt[lo];
-  const int ntok = (c + BN - 1) / BN;
-  const int local = t - tb.prefix[lo];
-  ti.f = local / ntok;
-  ti.n = local % ntok;
-  ti.d = lo / (E / h.s.world);
-  ti.row0 = tb.roff[lo] + ti.n * BN;
-  ti.valid = min(BN, c - ti.n * BN);
-  return ti;
-}
-
-__device__ __forceinline__ int n_mma(int valid) { return min(BN, (valid + 15) & ~15); }
-
-// Tables shared by both GEMM kinds (the fused pipeline runs both in one
-// launch): token tiles of BN rows per expert, tokprefix = exclusive prefix of
-// token tiles.  Kind k enumerates, per expert, f-major then token tile, so
-// its tile prefix is tokprefix * nf_k.
+// Per-expert tables for tile decoding, shared by both GEMM kinds (the fused
+// pipeline runs both in one launch): tokprefix = exclusive prefix of token
+// tiles.  Kind k enumerates, per expert, f-major then token tile, so its tile
+// prefix is tokprefix * nf_k.
 struct TokTables {
   int *cnt, *roff, *tokprefix;
 };
 __host__ __device__ constexpr size_t tok_tables_bytes(int num_experts) {
   return (size_t)(3 * num_experts + 1) * sizeof(int);
 }
+// Reads the dispatch results with __ldcg: in the fused pipeline they were
+// written earlier in the same launch.
 __device__ inline void build_tok_tables(const sym_heap &h, const TokTables &tb) {
   const int E = h.s.num_experts, E_loc = E / h.s.world;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -160,7 +132,7 @@ __device__ inline void build_tok_tables(const sym_heap &h, const TokTables &tb) 
     if (lane == 0) tb.tokprefix[0] = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
-      const int v = e < E ? (tb.cnt[e] + BN - 1) / BN : 0;
+      const int v = e < E ? ntok_of(tb.cnt[e]) : 0;
       int incl = v;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -183,13 +155,13 @@ __device__ inline TileInfo decode_tok(const sym_heap &h, const TokTables &tb, in
   TileInfo ti;
   ti.e = lo;
   const int c = tb.cnt[lo];
-  const int ntok = (c + BN - 1) / BN;
+  const int ntok = ntok_of(c);
   const int local = t - tb.tokprefix[lo] * nf;
   ti.f = local / ntok;
   ti.n = local % ntok;
   ti.d = lo / (E / h.s.world);
   ti.row0 = tb.roff[lo] + ti.n * BN;
-  ti.valid = min(BN, c - ti.n * BN);
+  ti.valid = ti.n == ntok - 1 ? c - ti.n * BN : BN;
   return ti;
 }
 
@@ -316,6 +288,275 @@ __device__ __forceinline__ void commit2_both(uint64_t *bar) {
           smem_u32(bar)),
       "h"(mask)
       : "memory");
+}
+
+
+// Static pair schedule over a list of tiles: wave i holds tiles
+// [i*npairs, (i+1)*npairs) (consecutive tiles share weight rows, so a wave
+// streams each weight block from HBM about once); pair p takes tile
+// i*npairs + (p+i) mod npairs of it.  The rotation keeps tiles that recur
+// with a period (every expert's last token tile, say) from landing on the
+// same few pairs.  Indices grow with i; only the last wave can run past the
+// end of the list.
+__device__ __forceinline__ int pair_tile(int i, int pair, int npairs) {
+  return i * npairs + (pair + i) % npairs;
+}
+
+// ---------------------------------------------------------------------------
+// The pair tile engine: the three roles of one tile, shared by the staged
+// expert GEMM and the fused pipeline.  Shared memory (both CTAs, same offsets):
+// a ring of STAGES stages [A 16 KB | B 16 KB | B1 2 KB] and the exchange
+// buffer; TMEM: two 256-column fp32 accumulators.  A tile whose rows exceed
+// BN (a remainder of <= REM_MAX rows on an expert's last tile) adds a second
+// MMA per K step on the remainder rows (B1) into the first columns of the
+// other accumulator, which it therefore also holds; its epilogue drains the
+// remainder first and hands that accumulator back before the main part.
+// ---------------------------------------------------------------------------
+struct Pipe {
+  uint8_t *ring;
+  float *xch;
+  uint64_t *full, *empty, *acc_full;
+  uint64_t *acc_empty;  // [2] accumulator b drained (main part of its tile)
+  uint64_t *acc_head;   // [2] its first 32 columns drained (where a remainder goes)
+  uint32_t tmem_base;
+  uint32_t rank;              // CTA rank in the pair (0: leader)
+  volatile int *abort;        // this CTA gives up (timeout or dependency failure)
+  const volatile int *stop;   // roles stop before tile index *stop
+  uint32_t tmo;               // wait limit, microseconds
+};
+
+__device__ __forceinline__ void ring_advance(int &stage, uint32_t &phase) {
+  if (++stage == STAGES) {
+    stage = 0;
+    phase ^= 1u;
+  }
+}
+
+struct ProdState {
+  int stage = 0;
+  uint32_t phase = 0;
+};
+
+// Producer K loop of one tile; TWO: the tile carries a remainder part (B1).
+// Templated so that no conditional copy sits in the loop.
+template <int KIND, bool TWO, typename Probe>
+__device__ __forceinline__ bool produce_k(const sym_heap &h, const Pipe &p, ProdState &s, int d, int arow,
+                                          int r0, int r1, const CUtensorMap *ma0, const CUtensorMap *ma1,
+                                          const CUtensorMap *mb0, const CUtensorMap *mb1, uint32_t tx, int t,
+                                          Probe &probe) {
+  const uint32_t full_leader = map_to(&p.full[0], 0);
+  const int nk = nk_of(h, KIND);
+  for (int kb = 0; kb < nk; ++kb) {
+    if (kb == nk / 2) probe();
+    if (!wait_or_stop(&p.empty[s.stage], s.phase ^ 1u, t, p.stop, p.abort, p.tmo, h)) return false;
+    uint8_t *sb = p.ring + (size_t)s.stage * STAGE_BYTES;
+    const uint32_t bar = full_leader + (uint32_t)(s.stage * sizeof(uint64_t));
+    if (p.rank == 0) mbar_arrive_expect_tx(&p.full[s.stage], tx);
+    if (KIND == GATE_UP) {
+      tma_load_2d_pair(sb, ma0, bar, kb * BK, arow);               // 64 gate rows
+      tma_load_2d_pair(sb + A_BYTES / 2, ma1, bar, kb * BK, arow);  // 64 up rows
+    } else {
+      tma_load_2d_pair(sb, ma0, bar, kb * BK, arow);  // 128 down rows
+    }
+    tma_load_3d_pair(sb + A_BYTES, mb0, bar, kb * BK, r0, d);
+    if (TWO) tma_load_3d_pair(sb + A_BYTES + B_BYTES, mb1, bar, kb * BK, r1, d);
+    ring_advance(s.stage, s.phase);
+  }
+  return true;
+}
+
+// Producer (one thread per CTA): streams tile ti's K blocks into the ring.
+// A rows from ma0 (gate or down rows) and ma1 (up rows), this CTA's token
+// rows from the box maps.  probe() runs once, halfway through the tile.
+template <int KIND, typename Probe>
+__device__ bool produce_tile(const sym_heap &h, const Pipe &p, ProdState &s, const TileInfo &ti,
+                             const CUtensorMap *ma0, const CUtensorMap *ma1, const BMaps &mb, int t,
+                             Probe probe) {
+  const TileGeom g = geom(ti.valid);
+  const int half0 = g.n0 / 2, half1 = g.n1 / 2;
+  const int box0 = box_index(half0), box1 = box_index(max(half1, 1));
+  const uint32_t b_rows = (uint32_t)(BOX_MIN_ROWS << box0) + (g.n1 ? (uint32_t)(BOX_MIN_ROWS << box1) : 0u);
+  const uint32_t tx = 2u * ((uint32_t)A_BYTES + b_rows * BK * 2);  // both CTAs' bytes
+  const int r0 = ti.row0 + (int)p.rank * half0;
+  const int r1 = ti.row0 + BN + (int)p.rank * half1;
+  const int arow = KIND == GATE_UP ? ti.e * h.s.inter + ti.f * 128 + (int)p.rank * 64
+                                   : ti.e * h.s.hidden + ti.f * 256 + (int)p.rank * 128;
+  return g.n1 ? produce_k<KIND, true>(h, p, s, ti.d, arow, r0, r1, ma0, ma1, &mb.m[box0], &mb.m[box1], tx, t,
+                                      probe)
+              : produce_k<KIND, false>(h, p, s, ti.d, arow, r0, r1, ma0, ma1, &mb.m[box0], &mb.m[box1], tx,
+                                       t, probe);
+}
+
+struct MmaState {
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t e0 = 0, e1 = 0;  // acquisitions of acc_empty[0] / [1] so far (main parts)
+  uint32_t h0 = 0, h1 = 0;  // acquisitions of acc_head[0] / [1] (main parts and remainders)
+  int abuf = 0;             // accumulator of the next tile's main part
+};
+
+// Acquisition n of a barrier waits for its release n-1 (releases never run
+// ahead of acquisitions, so the parity is unambiguous).
+__device__ __forceinline__ bool acquire(const sym_heap &h, const Pipe &p, uint64_t *bar, uint32_t &n, int t) {
+  const bool ok = wait_or_stop(bar, (n & 1u) ^ 1u, t, p.stop, p.abort, p.tmo, h);
+  ++n;
+  return ok;
+}
+
+// MMA K loop of one tile into d0 (and, TWO, the remainder into d1).
+template <int KIND, bool TWO>
+__device__ __forceinline__ bool mma_k(const sym_heap &h, const Pipe &p, MmaState &s, uint32_t d0, uint32_t d1,
+                                      uint32_t idesc0, uint32_t idesc1, int t) {
+  const int nk = nk_of(h, KIND);
+  for (int kb = 0; kb < nk; ++kb) {
+    if (!wait_or_stop(&p.full[s.stage], s.phase, t, p.stop, p.abort, p.tmo, h)) return false;
+    tc_fence_after();
+    uint8_t *sb = p.ring + (size_t)s.stage * STAGE_BYTES;
+    const uint64_t da = smem_desc_sw128(sb), db0 = smem_desc_sw128(sb + A_BYTES);
+    const uint64_t db1 = smem_desc_sw128(sb + A_BYTES + B_BYTES);
+#pragma unroll
+    for (int kk = 0; kk < BK / UK; ++kk) {
+      const uint64_t adv = (uint64_t)(kk * UK * 2 / 16);
+      const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+      mma2(d0, da + adv, db0 + adv, idesc0, acc);
+      if (TWO) mma2(d1, da + adv, db1 + adv, idesc1, acc);  // interleaved: issues faster than grouped
+    }
+    commit2_both(&p.empty[s.stage]);
+    ring_advance(s.stage, s.phase);
+  }
+  return true;
+}
+
+// MMA issuer (one thread of the leader CTA).
+template <int KIND>
+__device__ bool mma_tile(const sym_heap &h, const Pipe &p, MmaState &s, const TileInfo &ti, int t) {
+  const TileGeom g = geom(ti.valid);
+  const int b = s.abuf;
+  // main part: all of accumulator b; remainder: the first columns of the other
+  if (!acquire(h, p, &p.acc_empty[b], b ? s.e1 : s.e0, t)) return false;
+  if (!acquire(h, p, &p.acc_head[b], b ? s.h1 : s.h0, t)) return false;
+  if (g.n1 && !acquire(h, p, &p.acc_head[b ^ 1], b ? s.h0 : s.h1, t)) return false;
+  tc_fence_after();
+  const uint32_t d0 = p.tmem_base + (uint32_t)(b * ACC_COLS);
+  const uint32_t d1 = p.tmem_base + (uint32_t)((b ^ 1) * ACC_COLS);
+  const uint32_t idesc0 = idesc_bf16_f32(256, g.n0);
+  const bool ok = g.n1 ? mma_k<KIND, true>(h, p, s, d0, d1, idesc0, idesc_bf16_f32(256, g.n1), t)
+                       : mma_k<KIND, false>(h, p, s, d0, d1, idesc0, idesc0, t);
+  if (!ok) return false;
+  commit2_both(&p.acc_full[b]);
+  s.abuf = b ^ 1;
+  return true;
+}
+
+struct EpiState {
+  uint32_t used0 = 0, used1 = 0;  // tiles whose main part used each accumulator
+  int abuf = 0;
+};
+
+// hand (part of) an accumulator back to the leader's MMA: arrive once per
+// epilogue warp on the leader's barrier at this offset
+__device__ __forceinline__ void release_acc(const Pipe &p, uint64_t *bar, int lane) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) {
+    if (p.rank == 0) mbar_arrive(bar);
+    else mbar_arrive_remote(map_to(bar, 0));
+  }
+}
+
+// Epilogue of token rows [row, row + nrows) whose accumulators start at TMEM
+// address tcol (this warp's lane quarter q); head() runs once the first
+// 32 columns have been read.
+template <int KIND, typename Head>
+__device__ void epi_rows(const sym_heap &h, const Pipe &p, const TileInfo &ti, uint32_t tcol, int row,
+                         int nrows, int q, int lane, Head head) {
+  if (KIND == GATE_UP) {
+    const int pair = q & 1;  // gate lanes 32*pair.., up lanes 64 + 32*pair..
+    const bool is_gate = q < 2;
+    const int ld = h.s.inter;
+    const int feature = ti.f * 128 + (int)p.rank * 64 + pair * 32 + lane;
+    uint16_t *out = win<uint16_t>(h, ti.d, h.off_h) + (size_t)row * ld + feature;
+    // xch[pair][dir][16][32]: dir 0 carries up columns 0-15 to the gate warp,
+    // dir 1 gate columns 16-31 to the up warp
+    float *xb = p.xch + (size_t)pair * 2 * 16 * 32;
+    float *to_partner = xb + (is_gate ? 1 : 0) * 16 * 32;
+    const float *from_partner = xb + (is_gate ? 0 : 1) * 16 * 32;
+    for (int c0 = 0; c0 < nrows; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tcol + c0, v);
+      tmem_ld_wait();
+      if (c0 == 0) head();
+      xch_barrier(pair);  // the partner has read the previous chunk
+#pragma unroll
+      for (int c = 0; c < 16; ++c) to_partner[c * 32 + lane] = __uint_as_float(is_gate ? v[16 + c] : v[c]);
+      xch_barrier(pair);
+      const int keep = is_gate ? 0 : 16;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int col = c0 + keep + c;
+        const float other = from_partner[c * 32 + lane];
+        const float mine = __uint_as_float(is_gate ? v[c] : v[16 + c]);
+        const float gt = is_gate ? mine : other;
+        const float up = is_gate ? other : mine;
+        if (col < nrows) out[(size_t)col * ld] = to_bf16(__fdividef(gt, 1.0f + __expf(-gt)) * up);
+      }
+    }
+  } else {
+    const int ld = h.s.hidden;
+    const int feature = ti.f * 256 + (int)p.rank * 128 + q * 32 + lane;
+    uint16_t *out = win<uint16_t>(h, ti.d, h.off_y) + (size_t)row * ld + feature;
+    const bool live = feature < ld;  // a last feature tile may run past H
+    for (int c0 = 0; c0 < nrows; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tcol + c0, v);
+      tmem_ld_wait();
+      if (c0 == 0) head();
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (live && c0 + c < nrows) out[(size_t)(c0 + c) * ld] = to_bf16(__uint_as_float(v[c]));
+    }
+  }
+}
+
+// Epilogue warp (warps 2-5 of both CTAs; q = TMEM lane quarter).
+template <int KIND>
+__device__ bool epi_tile(const sym_heap &h, const Pipe &p, EpiState &s, const TileInfo &ti, int t, int q,
+                         int lane) {
+  const int b = s.abuf;
+  bool ok = wait_or_stop(&p.acc_full[b], (b ? s.used1 : s.used0) & 1u, t, p.stop, p.abort, p.tmo, h);
+  if (b) ++s.used1; else ++s.used0;
+  // warp-collective TMEM loads and the gate/up exchange follow: decide together
+  ok = KIND == GATE_UP ? xch_vote(q & 1, ok) : __all_sync(0xffffffffu, ok);
+  if (!ok) return false;
+  tc_fence_after();
+  const uint32_t lanes = p.tmem_base + ((uint32_t)(q * 32) << 16);
+  // part 1 (the remainder, in the other accumulator's first columns) first,
+  // then part 0; one copy of the drain code for both.  The first 32 columns of
+  // an accumulator are handed back as soon as they are read (the next tile's
+  // remainder may go there), the whole main accumulator at the end.
+  for (int part = ti.valid > BN ? 1 : 0; part >= 0; --part) {
+    const int buf = part ? (b ^ 1) : b;
+    epi_rows<KIND>(h, p, ti, lanes + (uint32_t)(buf * ACC_COLS), ti.row0 + part * BN,
+                   part ? ti.valid - BN : min(ti.valid, BN), q, lane,
+                   [&]() { release_acc(p, &p.acc_head[buf], lane); });
+    if (part == 0) release_acc(p, &p.acc_empty[buf], lane);
+  }
+  s.abuf = b ^ 1;
+  return true;
+}
+
+// Are the dispatched rows [row, row + n) of slot d in place?  (ready counter
+// per SYM_ROWS_PER_FLAG-row block; block=false only polls once)
+template <typename Wait>
+__device__ bool rows_ready(const sym_heap &h, int d, int row, int n, bool block, Wait wait) {
+  if (n <= 0) return true;
+  const int total = __ldcg(win<const int32_t>(h, d, h.off_total));
+  const uint32_t *ready = win<const uint32_t>(h, d, h.off_ready);
+  for (int b = row / SYM_ROWS_PER_FLAG; b <= (row + n - 1) / SYM_ROWS_PER_FLAG; ++b) {
+    const uint32_t target = (uint32_t)min(SYM_ROWS_PER_FLAG, total - b * SYM_ROWS_PER_FLAG);
+    if (block ? !wait(ready + b, target) : ld_acquire_u32(ready + b) < target) return false;
+  }
+  return true;
 }
 
 }  // namespace gemm2

@@ -113,3 +113,26 @@ def test_ragged_world_and_tokens_through_pipeline(sm):
     assert all(torch.equal(o.view(torch.int16), outs[0].view(torch.int16)) for o in outs)
     ref = oracle.pipeline(ms.logits_np(cfg), ms.x_np(cfg), cfg, fresh_weight_fn(cfg, DEV))
     assert_close(bits(outs[0]), bf16_f64(ref["out"]), "W=3 T=100 out")
+
+
+@pytest.mark.parametrize("fused", [0, 1])
+def test_remainder_rows_on_last_tile(sm, fused):
+    """Row counts around the token-tile boundary: 256 + r rows with r <= 32 put
+    the remainder on the one full tile (second MMA of the same weight stream),
+    r = 33 gets a tile of its own; 16, 512 + 20 and 256 + 1 rows cover one
+    short tile, a remainder behind two full tiles (a tile of its own) and the
+    smallest remainder."""
+    counts = [260, 288, 289, 16, 532, 257]
+    cfg = dict(world=2, tokens_per_slot=sum(counts) // 2, hidden=256, num_experts=6, topk=1, inter=384)
+    idx = np.repeat(np.arange(len(counts)), counts).reshape(-1, 1)
+    rng = np.random.default_rng(7)
+    idx = idx[rng.permutation(len(idx))]              # experts interleaved over the tokens
+    w = np.ones_like(idx, dtype=np.float32)
+    heap, out, w_used = _run(sm, cfg, idx, w, fused)
+    assert heap.status() == 0
+    ref = _oracle_from_idx(cfg, idx, w_used, fresh_weight_fn(cfg, DEV))
+    assert ref["cnt"].tolist() == counts
+    for d in range(cfg["world"]):
+        t = int(ref["tot"][d])
+        assert_close(bits(heap.y(d)[:t]), ref["y_exact"][d], f"slot {d} y")
+    assert_close(bits(out), bf16_f64(ref["out"]), "remainder tiles out")
