@@ -65,6 +65,20 @@ def max_over_ranks(value: float, world: int, device) -> float:
     return float(t.item())
 
 
+L2_BYTES = 129 * 2**20
+
+
+def l2_statement(cfg: dict) -> str:
+    """Whether one step's inputs alone exceed the 129 MB L2 (no flush needed)."""
+    wbytes = 3 * cfg["num_experts"] * cfg["hidden"] * cfg["inter"] * 2
+    n = cfg["world"] * cfg["tokens_per_slot"]
+    xbytes = n * cfg["hidden"] * 2 + n * cfg["num_experts"] * 4
+    if wbytes + xbytes > L2_BYTES:
+        return f"inputs larger than L2 (expert weights {wbytes / 2**20:.0f} MB, L2 129 MB); not flushed"
+    return (f"working set {(wbytes + xbytes) / 2**20:.1f} MB fits in L2 and is not flushed: "
+            "a small-case timing, not a roofline measurement")
+
+
 def workload_config(name: str, cfg: dict, fused: bool) -> dict:
     import moe_synth as ms
     n = cfg["world"] * cfg["tokens_per_slot"]
@@ -72,7 +86,7 @@ def workload_config(name: str, cfg: dict, fused: bool) -> dict:
             "world_slots": cfg["world"], "tokens_per_slot": cfg["tokens_per_slot"],
             "tokens_per_step": n, "hidden": cfg["hidden"], "inter": cfg["inter"],
             "experts": cfg["num_experts"], "topk": cfg["topk"], "fused": bool(fused),
-            "l2": "inputs larger than L2 (expert weights alone exceed 129 MB)",
+            "l2": l2_statement(cfg),
             "parallelism": "replicas"}
 
 
@@ -147,16 +161,26 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def traffic_record(kernel_file: str):
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
-    summary, or None if the kernel source changed since it was captured."""
+TRAFFIC_SOURCES = ("expert_ffn.cu", "gemm2sm.cuh", "symmoe_dev.cuh")
+
+
+def sources_sha256(files=TRAFFIC_SOURCES) -> str:
+    """sha256 over the kernel sources a traffic record was captured from."""
+    hsh = hashlib.sha256()
+    for f in files:
+        hsh.update(open(os.path.join(ROOT, "combine_symmetric_heap_gb300", "csrc", f), "rb").read())
+    return hsh.hexdigest()
+
+
+def traffic_record():
+    """Per-step DRAM bytes of the expert FFN launches from the committed ncu
+    summary, or None if any of their sources changed since it was captured."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
         rec = json.load(open(path))
-        src = open(os.path.join(ROOT, "combine_symmetric_heap_gb300", "csrc", kernel_file), "rb").read()
-        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
+        if rec.get("sources_sha256") != sources_sha256():
             return None
         return rec.get("traffic_bytes_per_step")
     except Exception:
@@ -379,7 +403,7 @@ def run_ours(args):
         other = {"tflops": alg["ffn_flops"] / kern_s / 1e12, "tensor_peak": tf_peak}
     other["frac"] = (other.get("hbm_gbs", 0) / hbm) if bound == "tensor" else other["tflops"] / tf_peak
     roofline = {"bound": bound, "kernel": kname, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": None if fused else traffic_record("expert_ffn.cu"),
+                "frac": achieved / peak, "traffic": None if fused else traffic_record(),
                 "peak_kind": f"{peak_src} " + ("bf16 " + ("sustained" if long_region else "burst")
                                                if bound == "tensor" else "HBM copy"),
                 "algorithmic_per_step": {"flops": alg["ffn_flops"], "bytes": alg["ffn_bytes"] + extra_bytes,
