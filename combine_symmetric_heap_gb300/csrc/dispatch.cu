@@ -10,17 +10,17 @@
 // ascending inside a slot; inside one expert by (source slot, token, k),
 // i.e. by global token g because the k experts of a token are distinct.
 //
-// Three launches (scan and scatter with programmatic dependent launch: each is
-// scheduled while its predecessor drains and waits for its results on the device):
+// Three launches, all with programmatic dependent launch (each is scheduled
+// while its predecessor drains and waits for that kernel's results on the device):
 //   count   one CTA per 128-token chunk: per-expert bitmask of the chunk's
 //           tokens in shared memory -> each pair's rank inside the chunk
 //           (popcount of the lower bits) and the chunk histogram.
 //   scan    one CTA: exclusive scan of the chunk histograms per expert (warp
 //           scans), expert counts, receive offsets per slot, total rows per
 //           slot; clears the ready counters for this call.
-//   scatter one CTA per token: x[g] is read once and stored k times (one per
-//           destination), then recv_pair / recv_w / pos are written and the
-//           ready counter of each destination row block is raised.
+//   scatter one 64-thread CTA per token: x[g] is read once and stored k times
+//           (one per destination), then recv_pair / recv_w / pos are written
+//           and the ready counter of each destination row block is raised.
 #include "symmoe_dev.cuh"
 
 namespace symmoe {
@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(CHUNK) dispatch_count_kernel(sym_heap h,
   const int t = threadIdx.x;
   const int g = chunk * CHUNK + t;
   pdl_launch_dependents();  // the scan may be scheduled now; it waits for this grid
+  pdl_wait();               // idx from the routing (or any earlier kernel)
   for (int i = t; i < E * (CHUNK / 32); i += CHUNK) mask[i] = 0;
   __syncthreads();
   const uint32_t bit = 1u << (t & 31);
@@ -117,9 +118,13 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(sym_heap h) {
     win<uint32_t>(h, i / h.num_ready, h.off_ready)[i % h.num_ready] = 0u;
 }
 
-constexpr int SCATTER_THREADS = 128;
-constexpr int SCATTER_VEC_PER_THREAD = 8;  // H <= 128*8*8 = 8192 in one pass
+// Scatter: a CTA of 64 threads per token, each thread holding VEC 16-byte
+// vectors of the row in registers between its load and its k stores.  Few
+// threads with many vectors keep more rows in flight per SM than many threads
+// with few (the register file, not the thread count, is the limit).
+constexpr int SCATTER_THREADS = 64;
 
+template <int VEC>
 __global__ void __launch_bounds__(SCATTER_THREADS)
     dispatch_scatter_kernel(sym_heap h, const uint4 *__restrict__ x,
                             const int32_t *__restrict__ idx, const float *__restrict__ w) {
@@ -135,10 +140,10 @@ __global__ void __launch_bounds__(SCATTER_THREADS)
   const uint4 *src = x + (size_t)g * nvec;
   pdl_wait();  // offsets from the scan; nothing is touched before it
 
-  // start the row loads before resolving the destinations
-  uint4 v[SCATTER_VEC_PER_THREAD];
+  // start the first pass's row loads before resolving the destinations
+  uint4 v[VEC];
 #pragma unroll
-  for (int i = 0; i < SCATTER_VEC_PER_THREAD; ++i) {
+  for (int i = 0; i < VEC; ++i) {
     const int c = tid + i * SCATTER_THREADS;
     if (c < nvec) v[i] = __ldg(src + c);
   }
@@ -167,18 +172,22 @@ __global__ void __launch_bounds__(SCATTER_THREADS)
     row_s[j] = p;
   }
   __syncthreads();
+  for (int base = 0;;) {
 #pragma unroll
-  for (int i = 0; i < SCATTER_VEC_PER_THREAD; ++i) {
-    const int c = tid + i * SCATTER_THREADS;
-    if (c < nvec)
-      for (int j = 0; j < k; ++j)
-        if (dst_s[j]) dst_s[j][c] = v[i];
-  }
-  // rows wider than one pass
-  for (int c = tid + SCATTER_VEC_PER_THREAD * SCATTER_THREADS; c < nvec; c += SCATTER_THREADS) {
-    const uint4 u = __ldg(src + c);
-    for (int j = 0; j < k; ++j)
-      if (dst_s[j]) dst_s[j][c] = u;
+    for (int i = 0; i < VEC; ++i) {
+      const int c = base + tid + i * SCATTER_THREADS;
+      if (c < nvec)
+        for (int j = 0; j < k; ++j)
+          if (dst_s[j]) dst_s[j][c] = v[i];
+    }
+    base += VEC * SCATTER_THREADS;
+    if (base >= nvec) break;
+    // rows wider than one pass
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const int c = base + tid + i * SCATTER_THREADS;
+      if (c < nvec) v[i] = __ldg(src + c);
+    }
   }
   if (tid < k && row_s[tid] >= 0) {
     const int d = slot_s[tid], p = row_s[tid];
@@ -199,14 +208,17 @@ cudaError_t launch_dispatch(const sym_heap &h, const uint16_t *x, const int32_t 
   const int N = h.s.world * h.s.tokens_per_slot;
   const int nchunks = (N + CHUNK - 1) / CHUNK;
   const size_t mask_bytes = (size_t)h.s.num_experts * (CHUNK / 32) * sizeof(uint32_t);
-  dispatch_count_kernel<<<nchunks, CHUNK, mask_bytes, st>>>(h, idx);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(dispatch_count_kernel, dim3(nchunks), dim3(CHUNK), mask_bytes, st, h, idx);
   if (err != cudaSuccess) return err;
   // scan and scatter are scheduled while their predecessor drains (they wait
   // for its results on the device)
   if ((err = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(1024), 0, st, h)) != cudaSuccess) return err;
-  return launch_pdl(dispatch_scatter_kernel, dim3(N), dim3(SCATTER_THREADS), 0, st, h,
-                    reinterpret_cast<const uint4 *>(x), idx, w);
+  // vectors per thread: the whole row in one pass up to H = 8192
+  const int nvec = h.s.hidden / 8;
+  auto kern = nvec <= 4 * SCATTER_THREADS   ? dispatch_scatter_kernel<4>
+              : nvec <= 8 * SCATTER_THREADS ? dispatch_scatter_kernel<8>
+                                            : dispatch_scatter_kernel<16>;
+  return launch_pdl(kern, dim3(N), dim3(SCATTER_THREADS), 0, st, h, reinterpret_cast<const uint4 *>(x), idx, w);
 }
 
 }  // namespace symmoe

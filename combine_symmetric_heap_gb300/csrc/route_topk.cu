@@ -17,6 +17,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict
                                                          int32_t *__restrict__ idx,
                                                          float *__restrict__ w, int n_tokens,
                                                          int n_experts, int k) {
+  pdl_launch_dependents();  // the dispatch count may be scheduled (it waits for idx)
   const int lane = threadIdx.x & 31;
   const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (g >= n_tokens) return;
