@@ -6,7 +6,8 @@
 // combine_in view (matching data_ptr) no staging copy is made, otherwise the
 // op silently copies first.  Both behaviours are here:
 //   combine_kernel        out[g] = bf16(sum_j w[g,j] * y[slot_j][pos[g,j]]),
-//                         fp32 fma in j order, 16-byte vector loads/stores;
+//                         fp32 fma in j order, 16-byte vector loads/stores,
+//                         the loads of up to four sources in flight together;
 //   stage_expert_out_kernel  the fallback copy of a caller's [W][cap][H]
 //                         expert output into the y windows (rows < total).
 #include "symmoe_dev.cuh"
@@ -15,6 +16,8 @@ namespace symmoe {
 
 constexpr int COMBINE_THREADS = 128;
 
+// G: sources whose loads are issued together before they are accumulated
+template <int G>
 __global__ void __launch_bounds__(COMBINE_THREADS)
     combine_kernel(sym_heap h, const int32_t *__restrict__ idx, const float *__restrict__ w,
                    uint4 *__restrict__ out) {
@@ -36,34 +39,45 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
   }
   __syncthreads();
   uint4 *dst = out + (size_t)g * nvec;
-  for (int c0 = tid; c0 < nvec; c0 += 2 * COMBINE_THREADS) {
-    float acc[2][8];
+  constexpr int U = 2;  // vectors per thread per pass
+  for (int c0 = tid; c0 < nvec; c0 += U * COMBINE_THREADS) {
+    float acc[U][8];
 #pragma unroll
-    for (int u = 0; u < 2; ++u)
+    for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const uint4 *s = src_s[j];
-      if (!s) continue;
-      const float wj = w_s[j];
+    for (int j0 = 0; j0 < k; j0 += G) {
+      // issue the loads of G sources first, then accumulate in j order
+      uint4 v[G][U];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = c0 + u * COMBINE_THREADS;
-        if (c < nvec) {
-          const uint4 v = __ldg(s + c);
-          acc[u][0] = fmaf(wj, bf16lo(v.x), acc[u][0]);
-          acc[u][1] = fmaf(wj, bf16hi(v.x), acc[u][1]);
-          acc[u][2] = fmaf(wj, bf16lo(v.y), acc[u][2]);
-          acc[u][3] = fmaf(wj, bf16hi(v.y), acc[u][3]);
-          acc[u][4] = fmaf(wj, bf16lo(v.z), acc[u][4]);
-          acc[u][5] = fmaf(wj, bf16hi(v.z), acc[u][5]);
-          acc[u][6] = fmaf(wj, bf16lo(v.w), acc[u][6]);
-          acc[u][7] = fmaf(wj, bf16hi(v.w), acc[u][7]);
+      for (int jj = 0; jj < G; ++jj) {
+        const uint4 *sp = j0 + jj < k ? src_s[j0 + jj] : nullptr;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int c = c0 + u * COMBINE_THREADS;
+          v[jj][u] = (sp && c < nvec) ? __ldg(sp + c) : make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < G; ++jj) {
+        if (j0 + jj >= k || !src_s[j0 + jj]) continue;
+        const float wj = w_s[j0 + jj];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const uint4 x = v[jj][u];
+          acc[u][0] = fmaf(wj, bf16lo(x.x), acc[u][0]);
+          acc[u][1] = fmaf(wj, bf16hi(x.x), acc[u][1]);
+          acc[u][2] = fmaf(wj, bf16lo(x.y), acc[u][2]);
+          acc[u][3] = fmaf(wj, bf16hi(x.y), acc[u][3]);
+          acc[u][4] = fmaf(wj, bf16lo(x.z), acc[u][4]);
+          acc[u][5] = fmaf(wj, bf16hi(x.z), acc[u][5]);
+          acc[u][6] = fmaf(wj, bf16lo(x.w), acc[u][6]);
+          acc[u][7] = fmaf(wj, bf16hi(x.w), acc[u][7]);
         }
       }
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int c = c0 + u * COMBINE_THREADS;
       if (c < nvec) {
         uint4 o;
@@ -99,7 +113,10 @@ cudaError_t launch_combine(const sym_heap &h, const uint16_t *expert_out, const 
     dim3 grid(num_sms * 2, h.s.world);
     stage_expert_out_kernel<<<grid, 256, 0, st>>>(h, reinterpret_cast<const uint4 *>(expert_out));
   }
-  combine_kernel<<<N, COMBINE_THREADS, 0, st>>>(h, idx, w, reinterpret_cast<uint4 *>(out));
+  if (h.s.topk <= 2)
+    combine_kernel<2><<<N, COMBINE_THREADS, 0, st>>>(h, idx, w, reinterpret_cast<uint4 *>(out));
+  else
+    combine_kernel<4><<<N, COMBINE_THREADS, 0, st>>>(h, idx, w, reinterpret_cast<uint4 *>(out));
   return cudaGetLastError();
 }
 
