@@ -45,6 +45,7 @@ constexpr int EPI_WARPS_PER_TILE = 8;  // 4 epilogue warps in each CTA of a pair
 constexpr int FUSED_CHUNK = 32;  // tokens per route+count task (one bitmask word per expert)
 constexpr int SCATTER_TOKENS = 8;  // tokens per scatter task (one warp each)
 constexpr int COMBINE_TOKENS = 8;  // tokens per combine task
+constexpr int SCATTER_SLOTS_MAX = 3;  // rows a warp stages in shared memory at once (scatter)
 constexpr int FUSED_CTRL_SMEM = 512;
 
 // control words in slot 0's ctrl window
@@ -53,6 +54,7 @@ enum Ctl : int {
   C_ROUTE_DONE = 1,
   C_SCAN_DONE = 2,  // epoch of the last completed scan
   C_SCATTER_NEXT = 3,
+  C_SCATTER_DONE = 4,  // scatter tasks completed (pos final for the combine)
   C_COMB_NEXT = 6,
   C_EXIT = 7,
   C_ABORT = 8,
@@ -284,8 +286,85 @@ __device__ inline void scatter_token(const sym_heap &h, const FusedArgs &a, int 
   __syncwarp();
 }
 
+// Scatter of up to `slots` consecutive tokens by one warp through its share of
+// the (idle) GEMM ring: lanes < k resolve each token's destinations; lane 0
+// bulk-loads every row into its slot and, as each lands, bulk-stores it to
+// the row's k destinations; once all copies are complete it releases the
+// ready counters of the destination row blocks.  Rows move by the copy
+// engine, so a warp keeps `slots` rows in flight without holding them in
+// registers.  Returns false if a row load did not complete in time.
+__device__ inline bool scatter_bulk(const sym_heap &h, const FusedArgs &a, int g0, int slots, uint8_t *wring,
+                                    uint64_t *sbar, uint32_t &sph, int lane, uint4 **dst_s) {
+  const int E = h.s.num_experts, k = h.s.topk, T = h.s.tokens_per_slot, H = h.s.hidden;
+  const int E_loc = E / h.s.world;
+  const int N = h.s.world * T;
+  const int nchunks = (N + FUSED_CHUNK - 1) / FUSED_CHUNK;
+  const uint32_t rowbytes = (uint32_t)H * 2;
+  int dd[SCATTER_SLOTS_MAX], pp[SCATTER_SLOTS_MAX];
+#pragma unroll
+  for (int s = 0; s < SCATTER_SLOTS_MAX; ++s) {
+    dd[s] = 0;
+    pp[s] = -1;
+    const int g = g0 + s;
+    if (s < slots && g < N && lane < k) {
+      int32_t *pos = win<int32_t>(h, g / T, h.off_pos) + (size_t)(g % T) * k;
+      const int e = __ldcg(a.idx + (size_t)g * k + lane);
+      const int d = e / E_loc;
+      int p = __ldcg(win<int32_t>(h, d, h.off_recv_off) + e % E_loc) +
+              __ldcg(win<int32_t>(h, 0, h.off_hist) + (size_t)e * nchunks + g / FUSED_CHUNK) + __ldcg(pos + lane);
+      uint4 *dst = nullptr;
+      if (p < 0 || (uint64_t)p >= h.cap) {
+        raise_status(h, SYM_STATUS_OVERFLOW);
+        p = -1;
+      } else {
+        dst = win<uint4>(h, d, h.off_recv_x) + (size_t)p * (H / 8);
+        win<int32_t>(h, d, h.off_recv_pair)[p] = g * k + lane;
+        win<float>(h, d, h.off_recv_w)[p] = __ldcg(a.w + (size_t)g * k + lane);
+      }
+      pos[lane] = p;
+      dst_s[s * 32 + lane] = dst;
+      dd[s] = d;
+      pp[s] = p;
+    }
+  }
+  __syncwarp();
+  const int nrows = max(0, min(slots, N - g0));
+  bool ok = true;
+  if (lane == 0) {
+    for (int s = 0; s < nrows; ++s) {
+      mbar_arrive_expect_tx(&sbar[s], rowbytes);
+      bulk_load(wring + (size_t)s * rowbytes, a.x + (size_t)(g0 + s) * H, rowbytes, &sbar[s]);
+    }
+    for (int s = 0; s < nrows && ok; ++s) {
+      ok = mbar_wait(&sbar[s], (sph >> s) & 1u, h.wait_timeout_us, nullptr);
+      if (ok)
+        for (int j = 0; j < k; ++j)
+          if (dst_s[s * 32 + j]) bulk_store(dst_s[s * 32 + j], wring + (size_t)s * rowbytes, rowbytes);
+    }
+    bulk_commit();
+    bulk_wait_all();
+    // the rows were written by the async proxy; order them before the release
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __threadfence();
+  }
+  sph ^= (1u << nrows) - 1u;
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  if (!ok) return false;
+#pragma unroll
+  for (int s = 0; s < SCATTER_SLOTS_MAX; ++s) {
+    if (s >= nrows) break;
+    for (int j = 0; j < k; ++j) {
+      const int pj = __shfl_sync(0xffffffffu, pp[s], j), dj = __shfl_sync(0xffffffffu, dd[s], j);
+      if (lane == 0 && pj >= 0) atomicAdd(win<uint32_t>(h, dj, h.off_ready) + pj / SYM_ROWS_PER_FLAG, 1u);
+    }
+  }
+  __syncwarp();
+  return true;
+}
+
 // ---------------------------------------------------------------- phase 4
 // One warp per token; src_s / w_s are this warp's 32-entry tables.
+template <int U, int G>
 __device__ inline void combine_token(const sym_heap &h, const FusedArgs &a, const gemm2::TokTables &tb,
                                      int g, int lane, const uint4 **src_s, float *w_s) {
   const int E = h.s.num_experts, k = h.s.topk, T = h.s.tokens_per_slot, H = h.s.hidden;
@@ -308,30 +387,56 @@ __device__ inline void combine_token(const sym_heap &h, const FusedArgs &a, cons
   }
   if (!__all_sync(0xffffffffu, ok)) return;
   uint4 *dst = reinterpret_cast<uint4 *>(a.out) + (size_t)g * (H / 8);
-  for (int c = lane; c < H / 8; c += 32) {
-    float acc[8];
+  const int nvec = H / 8;
+  // U vectors per lane per pass, the loads of G sources issued together, then
+  // accumulated in j order (the staged combine's order)
+  for (int c0 = lane; c0 < nvec; c0 += 32 * U) {
+    float acc[U][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const uint4 *sj = src_s[j];
-      if (!sj) continue;
-      const float ww = w_s[j];
-      const uint4 v = __ldcg(sj + c);
-      acc[0] = fmaf(ww, bf16lo(v.x), acc[0]);
-      acc[1] = fmaf(ww, bf16hi(v.x), acc[1]);
-      acc[2] = fmaf(ww, bf16lo(v.y), acc[2]);
-      acc[3] = fmaf(ww, bf16hi(v.y), acc[3]);
-      acc[4] = fmaf(ww, bf16lo(v.z), acc[4]);
-      acc[5] = fmaf(ww, bf16hi(v.z), acc[5]);
-      acc[6] = fmaf(ww, bf16lo(v.w), acc[6]);
-      acc[7] = fmaf(ww, bf16hi(v.w), acc[7]);
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+    for (int j0 = 0; j0 < k; j0 += G) {
+      uint4 v[G][U];
+#pragma unroll
+      for (int jj = 0; jj < G; ++jj) {
+        const uint4 *sp = j0 + jj < k ? src_s[j0 + jj] : nullptr;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int c = c0 + 32 * u;
+          v[jj][u] = (sp && c < nvec) ? __ldcg(sp + c) : make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < G; ++jj) {
+        if (j0 + jj >= k || !src_s[j0 + jj]) continue;
+        const float ww = w_s[j0 + jj];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const uint4 x = v[jj][u];
+          acc[u][0] = fmaf(ww, bf16lo(x.x), acc[u][0]);
+          acc[u][1] = fmaf(ww, bf16hi(x.x), acc[u][1]);
+          acc[u][2] = fmaf(ww, bf16lo(x.y), acc[u][2]);
+          acc[u][3] = fmaf(ww, bf16hi(x.y), acc[u][3]);
+          acc[u][4] = fmaf(ww, bf16lo(x.z), acc[u][4]);
+          acc[u][5] = fmaf(ww, bf16hi(x.z), acc[u][5]);
+          acc[u][6] = fmaf(ww, bf16lo(x.w), acc[u][6]);
+          acc[u][7] = fmaf(ww, bf16hi(x.w), acc[u][7]);
+        }
+      }
     }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    dst[c] = o;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + 32 * u;
+      if (c < nvec) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+        o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+        o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+        o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+        dst[c] = o;
+      }
+    }
   }
   __syncwarp();
 }
@@ -356,6 +461,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
   volatile int *abort_s = reinterpret_cast<volatile int *>(tmem_base_s + 1);
   volatile int *never_s = abort_s + 1;  // "stop before tile" bound: never
   int *bcast = const_cast<int *>(never_s + 1);
+  // per-warp row-slot barriers of the scatter phase
+  uint64_t *sbar = reinterpret_cast<uint64_t *>(ctrl_s + 256) + warp_id() * SCATTER_SLOTS_MAX;
   const int E = h.s.num_experts;
   int *tab = reinterpret_cast<int *>(ctrl_s + FUSED_CTRL_SMEM);
   const TokTables tb{tab, tab + E, tab + 2 * E};
@@ -391,6 +498,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
       mbar_init(&p.acc_head[b], 8);
     }
     mbar_init(drained, 1);
+    uint64_t *sbar0 = reinterpret_cast<uint64_t *>(ctrl_s + 256);
+    for (int i = 0; i < FUSED_THREADS / 32 * SCATTER_SLOTS_MAX; ++i) mbar_init(&sbar0[i], 1);
     *abort_s = 0;
     *never_s = 0x7fffffff;
     fence_mbar_init();
@@ -428,16 +537,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
   if (threadIdx.x == 0) *bcast = wait_geq(h, ctl(h) + C_SCAN_DONE, h.epoch) ? 1 : 0;
   __syncthreads();
   const bool scanned = *bcast != 0 && ld_acquire_u32(ctl(h) + C_SCAN_DONE) == h.epoch;
-  if (scanned) {
-    const int ntask = (N + SCATTER_TOKENS - 1) / SCATTER_TOKENS;
+  // rows per warp staged in its share of the ring (0: rows too wide, plain copies)
+  const size_t warp_ring = (size_t)STAGES * STAGE_BYTES / (FUSED_THREADS / 32);
+  const int slots = min(SCATTER_SLOTS_MAX, (int)(warp_ring / ((size_t)h.s.hidden * 2)));
+  const int scatter_tasks = slots > 0 ? (N + FUSED_THREADS / 32 * slots - 1) / (FUSED_THREADS / 32 * slots)
+                                      : (N + SCATTER_TOKENS - 1) / SCATTER_TOKENS;
+  int tasks_done = 0;
+  if (scanned && slots > 0) {
+    // the ring held phase 1's logits rows (generic stores); the copy engine writes it next
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    const int per_task = FUSED_THREADS / 32 * slots;
+    const int ntask = scatter_tasks;
+    uint4 **dst_tab = reinterpret_cast<uint4 **>(xch_raw) + wid * SCATTER_SLOTS_MAX * 32;
+    uint32_t sph = 0;
     for (;;) {
       const int t = claim(h, C_SCATTER_NEXT, bcast);
       if (t >= ntask) break;
+      if (!scatter_bulk(h, a, t * per_task + wid * slots, slots, ring + wid * warp_ring, sbar, sph, lane,
+                        dst_tab))
+        set_abort(h);
+      ++tasks_done;
+    }
+  } else if (scanned) {
+    for (;;) {
+      const int t = claim(h, C_SCATTER_NEXT, bcast);
+      if (t >= scatter_tasks) break;
       for (int i = wid; i < SCATTER_TOKENS; i += FUSED_THREADS / 32) {
         const int g = t * SCATTER_TOKENS + i;
         if (g < N) scatter_token(h, a, g, lane, reinterpret_cast<uint4 **>(ptr_s));
       }
+      ++tasks_done;
     }
+  }
+  // publish this CTA's completed scatter tasks (release of its pos / row writes)
+  __syncthreads();
+  if (threadIdx.x == 0 && tasks_done > 0) {
+    __threadfence();
+    atomicAdd(ctl(h) + C_SCATTER_DONE, (uint32_t)tasks_done);
   }
 
   // ---------------- phase 3: expert GEMM tiles on the CTA pair
@@ -539,16 +675,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
   __syncthreads();
 
   // ---------------- phase 4: combine
-  if (scanned) {
+  // every token's pos is final once all scatter tasks are done (a CTA with no
+  // GEMM tiles gets here while other CTAs may still be scattering)
+  if (threadIdx.x == 0)
+    *bcast = scanned && wait_geq(h, ctl(h) + C_SCATTER_DONE, (uint32_t)scatter_tasks) ? 1 : 0;
+  __syncthreads();
+  if (*bcast) {
     const int ntask = (N + COMBINE_TOKENS - 1) / COMBINE_TOKENS;
     for (;;) {
       const int t = claim(h, C_COMB_NEXT, bcast);
       if (t >= ntask) break;
       for (int i = wid; i < COMBINE_TOKENS; i += FUSED_THREADS / 32) {
         const int g = t * COMBINE_TOKENS + i;
-        if (g < N)
-          combine_token(h, a, tb, g, lane, reinterpret_cast<const uint4 **>(const_cast<const void **>(ptr_s)),
-                        wgt_s);
+        if (g >= N) continue;
+        const uint4 **src_tab = reinterpret_cast<const uint4 **>(const_cast<const void **>(ptr_s));
+        if (h.s.topk <= 2)
+          combine_token<8, 2>(h, a, tb, g, lane, src_tab, wgt_s);
+        else
+          combine_token<4, 4>(h, a, tb, g, lane, src_tab, wgt_s);
       }
     }
   }
@@ -567,6 +711,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
       c[C_ROUTE_NEXT] = 0;
       c[C_ROUTE_DONE] = 0;
       c[C_SCATTER_NEXT] = 0;
+      c[C_SCATTER_DONE] = 0;
       c[C_COMB_NEXT] = 0;
       c[C_ABORT] = 0;
       __threadfence();
@@ -590,8 +735,10 @@ cudaError_t launch_fused(const sym_heap &h, const float *logits, const uint16_t 
       !encode_heap_boxes(&trx, h, h.off_recv_x, H) ||
       !encode_2d(&td, wd, (uint64_t)E * H, I, 128) || !encode_heap_boxes(&th, h, h.off_h, I))
     return cudaErrorInvalidValue;
-  static_assert(FUSED_THREADS / 32 * 32 * (sizeof(void *) + sizeof(float)) <= (size_t)XCH_BYTES,
+  static_assert(FUSED_THREADS / 32 * 32 * (sizeof(void *) + sizeof(float)) <= (size_t)XCH_BYTES &&
+                    FUSED_THREADS / 32 * SCATTER_SLOTS_MAX * 32 * sizeof(void *) <= (size_t)XCH_BYTES,
                 "per-warp tables live in the exchange buffer");
+  static_assert(256 + FUSED_THREADS / 32 * SCATTER_SLOTS_MAX * 8 <= FUSED_CTRL_SMEM, "scatter barriers");
   const size_t smem = 1024 + (size_t)STAGES * STAGE_BYTES + XCH_BYTES + FUSED_CTRL_SMEM +
                       tok_tables_bytes(E);
   cudaError_t err = cudaFuncSetAttribute(moe_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
