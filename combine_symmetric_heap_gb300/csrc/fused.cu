@@ -7,11 +7,13 @@
 // launch.  Here the four stages run in one launch (CTAs in clusters of two,
 // one per SM, all resident) and overlap per tile:
 //
-//   phase 1  route + count, one task per 32-token chunk: route the chunk
-//            (logits rows staged in shared memory), then per-expert bitmasks
-//            give every pair its rank in the chunk and the chunk histogram.
-//            The CTA that completes the last chunk runs the scan (counts,
-//            receive offsets, totals) and clears the readiness counters, then
+//   phase 1  route + count: route tasks of a 32-token chunk, or of one token
+//            per warp when there are fewer chunks than CTAs (logits rows
+//            staged in shared memory); the CTA that finishes the last route
+//            task of a 32-token chunk counts the chunk (per-expert bitmasks give
+//            every pair its rank in the chunk and the chunk histogram).  The
+//            CTA that counts the last chunk runs the scan (counts, receive
+//            offsets, totals) and clears the readiness counters, then
 //            publishes scan_done = epoch.
 //   phase 2  scatter, one warp per token: rows go straight into the
 //            destination slot's recv_x window; each row raises the ready
@@ -42,7 +44,8 @@ namespace symmoe {
 
 constexpr int FUSED_THREADS = 256;  // warps 0-5 run the GEMM roles, all 8 the memory phases
 constexpr int EPI_WARPS_PER_TILE = 8;  // 4 epilogue warps in each CTA of a pair
-constexpr int FUSED_CHUNK = 32;  // tokens per route+count task (one bitmask word per expert)
+constexpr int FUSED_CHUNK = 32;  // tokens per count chunk (one bitmask word per expert)
+constexpr int ROUTE_TOKENS = 8;  // tokens per route task with few chunks (one per warp)
 constexpr int SCATTER_TOKENS = 8;  // tokens per scatter task (one warp each)
 constexpr int COMBINE_TOKENS = 8;  // tokens per combine task
 constexpr int SCATTER_SLOTS_MAX = 3;  // rows a warp stages in shared memory at once (scatter)
@@ -79,6 +82,10 @@ __device__ __forceinline__ uint32_t *ctl(const sym_heap &h) { return win<uint32_
 __device__ __forceinline__ uint32_t *h_ready(const sym_heap &h) { return ctl(h) + C_WORDS; }
 __device__ __forceinline__ uint32_t *y_ready(const sym_heap &h) {
   return ctl(h) + C_WORDS + fused_h_blocks(h.s);
+}
+// route tasks finished per count chunk
+__device__ __forceinline__ uint32_t *chunk_done(const sym_heap &h) {
+  return y_ready(h) + fused_y_blocks(h.s);
 }
 __device__ __forceinline__ bool global_abort(const sym_heap &h) {
   return *reinterpret_cast<volatile uint32_t *>(ctl(h) + C_ABORT) != 0;
@@ -157,19 +164,15 @@ __device__ inline void route_token(float *row, int E, int k, int32_t *idx_out, f
   }
 }
 
-// Route the 32 tokens of a chunk (4 per warp), then rank each pair inside the
-// chunk by the per-expert bitmask and write the chunk histogram.
-// smem: 8 logits rows of E floats, then the E mask words.
-__device__ inline void route_count_chunk(const sym_heap &h, const FusedArgs &a, int chunk,
-                                         float *smem) {
-  const int E = h.s.num_experts, k = h.s.topk, T = h.s.tokens_per_slot;
-  const int N = h.s.world * T;
-  const int nchunks = (N + FUSED_CHUNK - 1) / FUSED_CHUNK;
+// Route the rt tokens of a route task, rt / 8 per warp (logits rows staged in
+// shared memory).
+__device__ inline void route_task(const sym_heap &h, const FusedArgs &a, int task, int rt, float *smem) {
+  const int E = h.s.num_experts, k = h.s.topk;
+  const int N = h.s.world * h.s.tokens_per_slot;
   const int wid = warp_id(), lane = lane_id(), nw = blockDim.x >> 5;
   float *row = smem + (size_t)wid * E;
-  uint32_t *mask = reinterpret_cast<uint32_t *>(smem + (size_t)nw * E);
-  for (int t = wid; t < FUSED_CHUNK; t += nw) {
-    const int g = chunk * FUSED_CHUNK + t;
+  for (int i = wid; i < rt; i += nw) {
+    const int g = task * rt + i;
     if (g >= N) break;
     const float *src = a.logits + (size_t)g * E;
     for (int e = lane; e < E; e += 32) row[e] = __ldg(src + e);
@@ -177,6 +180,16 @@ __device__ inline void route_count_chunk(const sym_heap &h, const FusedArgs &a, 
     route_token(row, E, k, a.idx + (size_t)g * k, a.w + (size_t)g * k, lane);
     __syncwarp();
   }
+}
+
+// Rank each pair of a 32-token chunk inside the chunk by the per-expert
+// bitmask and write the chunk histogram.  The routes of the chunk were
+// written by other CTAs of this launch (read with __ldcg after an acquire).
+// smem: E mask words.
+__device__ inline void count_chunk(const sym_heap &h, const FusedArgs &a, int chunk, uint32_t *mask) {
+  const int E = h.s.num_experts, k = h.s.topk, T = h.s.tokens_per_slot;
+  const int N = h.s.world * T;
+  const int nchunks = (N + FUSED_CHUNK - 1) / FUSED_CHUNK;
   for (int i = threadIdx.x; i < E; i += blockDim.x) mask[i] = 0;
   __syncthreads();
   const int t = threadIdx.x;
@@ -184,11 +197,11 @@ __device__ inline void route_count_chunk(const sym_heap &h, const FusedArgs &a, 
   const uint32_t bit = 1u << t;
   if (t < FUSED_CHUNK && g < N)
     for (int j = 0; j < k; ++j)
-      if (atomicOr(&mask[a.idx[(size_t)g * k + j]], bit) & bit) raise_status(h, SYM_STATUS_OVERFLOW);
+      if (atomicOr(&mask[__ldcg(a.idx + (size_t)g * k + j)], bit) & bit) raise_status(h, SYM_STATUS_OVERFLOW);
   __syncthreads();
   if (t < FUSED_CHUNK && g < N) {
     int32_t *pos = win<int32_t>(h, g / T, h.off_pos) + (size_t)(g % T) * k;
-    for (int j = 0; j < k; ++j) pos[j] = __popc(mask[a.idx[(size_t)g * k + j]] & (bit - 1u));
+    for (int j = 0; j < k; ++j) pos[j] = __popc(mask[__ldcg(a.idx + (size_t)g * k + j)] & (bit - 1u));
   }
   int32_t *hist = win<int32_t>(h, 0, h.off_hist);
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)e * nchunks + chunk] = __popc(mask[e]);
@@ -233,6 +246,7 @@ __device__ inline void scan_and_publish(const sym_heap &h, int32_t *cnt_s) {
   const int nh = fused_h_blocks(h.s), ny = fused_y_blocks(h.s);
   for (int i = threadIdx.x; i < nh; i += blockDim.x) h_ready(h)[i] = 0u;
   for (int i = threadIdx.x; i < ny; i += blockDim.x) y_ready(h)[i] = 0u;
+  for (int i = threadIdx.x; i < nchunks; i += blockDim.x) chunk_done(h)[i] = 0u;  // all counted
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -441,6 +455,94 @@ __device__ inline void combine_token(const sym_heap &h, const FusedArgs &a, cons
   __syncwarp();
 }
 
+// Combine of one token by one warp, its sources streamed through the warp's
+// share of the (idle) GEMM ring with cp.async: per pass each lane copies U
+// vectors of every source into shared memory, double-buffered, so the next
+// pass is in flight while this one is accumulated (in j order).  k <= KMAX.
+template <int U, int KMAX>
+__device__ inline void combine_token_stream(const sym_heap &h, const FusedArgs &a, const gemm2::TokTables &tb,
+                                            int g, int lane, const uint4 **src_s, float *w_s, uint4 *buf) {
+  const int E = h.s.num_experts, k = h.s.topk, T = h.s.tokens_per_slot, H = h.s.hidden;
+  const int E_loc = E / h.s.world;
+  const uint32_t target = EPI_WARPS_PER_TILE * (uint32_t)gemm2::nf_of(h, gemm2::DOWN);
+  bool ok = true;
+  if (lane < k) {
+    const int e = __ldcg(a.idx + (size_t)g * k + lane);
+    const int p = __ldcg(win<const int32_t>(h, g / T, h.off_pos) + (size_t)(g % T) * k + lane);
+    const uint4 *src = nullptr;
+    if (p >= 0) {
+      ok = wait_geq(h, y_ready(h) + tb.tokprefix[e] + gemm2::tile_of_row(tb.cnt[e], p - tb.roff[e]), target);
+      src = win<const uint4>(h, e / E_loc, h.off_y) + (size_t)p * (H / 8);
+    }
+    src_s[lane] = src;
+    w_s[lane] = __ldcg(a.w + (size_t)g * k + lane);
+  }
+  if (!__all_sync(0xffffffffu, ok)) return;
+  uint4 *dst = reinterpret_cast<uint4 *>(a.out) + (size_t)g * (H / 8);
+  const int nvec = H / 8, step = 32 * U;
+  const int npass = (nvec + step - 1) / step;
+  // buf[b][j][u][lane]
+  auto slot = [&](int b, int j, int u) { return buf + (((size_t)b * KMAX + j) * U + u) * 32 + lane; };
+  auto issue = [&](int pass, int b) {
+    for (int j = 0; j < k; ++j) {
+      const uint4 *sp = src_s[j];
+      if (!sp) continue;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = pass * step + u * 32 + lane;
+        if (c < nvec) cp_async16(slot(b, j, u), sp + c);
+      }
+    }
+    cp_async_commit();
+  };
+  issue(0, 0);
+  for (int pass = 0; pass < npass; ++pass) {
+    if (pass + 1 < npass) {
+      issue(pass + 1, (pass + 1) & 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    const int b = pass & 1;
+    float acc[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      if (!src_s[j]) continue;
+      const float ww = w_s[j];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = pass * step + u * 32 + lane;
+        if (c >= nvec) continue;
+        const uint4 x = *slot(b, j, u);
+        acc[u][0] = fmaf(ww, bf16lo(x.x), acc[u][0]);
+        acc[u][1] = fmaf(ww, bf16hi(x.x), acc[u][1]);
+        acc[u][2] = fmaf(ww, bf16lo(x.y), acc[u][2]);
+        acc[u][3] = fmaf(ww, bf16hi(x.y), acc[u][3]);
+        acc[u][4] = fmaf(ww, bf16lo(x.z), acc[u][4]);
+        acc[u][5] = fmaf(ww, bf16hi(x.z), acc[u][5]);
+        acc[u][6] = fmaf(ww, bf16lo(x.w), acc[u][6]);
+        acc[u][7] = fmaf(ww, bf16hi(x.w), acc[u][7]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = pass * step + u * 32 + lane;
+      if (c < nvec) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+        o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+        o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+        o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+        dst[c] = o;
+      }
+    }
+  }
+  __syncwarp();
+}
+
 // ---------------------------------------------------------------- kernel
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
     moe_fused_kernel(const sym_heap h, const FusedArgs a, const __grid_constant__ CUtensorMap tm_g,
@@ -522,15 +624,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
   p.tmem_base = *tmem_base_s;
 
   // ---------------- phase 1: route + count (the last finisher scans)
-  for (;;) {
-    const int c = claim(h, C_ROUTE_NEXT, bcast);
-    if (c >= nchunks) break;
-    route_count_chunk(h, a, c, reinterpret_cast<float *>(ring));
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) *bcast = (int)atomicAdd(ctl(h) + C_ROUTE_DONE, 1u);
-    __syncthreads();
-    if (*bcast == nchunks - 1) scan_and_publish(h, reinterpret_cast<int32_t *>(ring));
+  // Route tasks of rt tokens: a whole 32-token chunk when there are chunks
+  // for every CTA, else one token per warp (short batches).  The CTA finishing
+  // the last route task of a chunk counts that chunk; the CTA counting the
+  // last chunk scans.
+  {
+    const int rt = nchunks >= (int)gridDim.x ? FUSED_CHUNK : ROUTE_TOKENS;
+    const int nroute = (N + rt - 1) / rt;
+    const int tasks_per_chunk = FUSED_CHUNK / rt;
+    for (;;) {
+      const int t = claim(h, C_ROUTE_NEXT, bcast);
+      if (t >= nroute) break;
+      route_task(h, a, t, rt, reinterpret_cast<float *>(ring));
+      const int c = t / tasks_per_chunk;
+      const int in_chunk = min(tasks_per_chunk, (min(N, (c + 1) * FUSED_CHUNK) - c * FUSED_CHUNK + rt - 1) / rt);
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        __threadfence();  // release this task's routes
+        *bcast = (int)atomicAdd(chunk_done(h) + c, 1u) == in_chunk - 1;
+        __threadfence();  // acquire the chunk's other routes
+      }
+      __syncthreads();
+      if (!*bcast) continue;
+      count_chunk(h, a, c, reinterpret_cast<uint32_t *>(ring) + (FUSED_THREADS / 32) * h.s.num_experts);
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) *bcast = (int)atomicAdd(ctl(h) + C_ROUTE_DONE, 1u);
+      __syncthreads();
+      if (*bcast == nchunks - 1) scan_and_publish(h, reinterpret_cast<int32_t *>(ring));
+    }
   }
 
   // ---------------- phase 2: scatter
@@ -679,6 +801,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
   // GEMM tiles gets here while other CTAs may still be scattering)
   if (threadIdx.x == 0)
     *bcast = scanned && wait_geq(h, ctl(h) + C_SCATTER_DONE, (uint32_t)scatter_tasks) ? 1 : 0;
+  // the ring was last touched by the async proxy (TMA, MMA); cp.async writes it next
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
   if (*bcast) {
     const int ntask = (N + COMBINE_TOKENS - 1) / COMBINE_TOKENS;
@@ -689,8 +813,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
         const int g = t * COMBINE_TOKENS + i;
         if (g >= N) continue;
         const uint4 **src_tab = reinterpret_cast<const uint4 **>(const_cast<const void **>(ptr_s));
+        uint4 *cbuf = reinterpret_cast<uint4 *>(ring + wid * warp_ring);
         if (h.s.topk <= 2)
-          combine_token<8, 2>(h, a, tb, g, lane, src_tab, wgt_s);
+          combine_token_stream<8, 2>(h, a, tb, g, lane, src_tab, wgt_s, cbuf);
+        else if (h.s.topk <= 4)
+          combine_token_stream<6, 4>(h, a, tb, g, lane, src_tab, wgt_s, cbuf);
+        else if (h.s.topk <= 8)
+          combine_token_stream<3, 8>(h, a, tb, g, lane, src_tab, wgt_s, cbuf);
         else
           combine_token<4, 4>(h, a, tb, g, lane, src_tab, wgt_s);
       }
@@ -721,7 +850,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
 }
 
 size_t fused_ctrl_bytes(const moe_shape &s) {
-  return (size_t)(C_WORDS + fused_h_blocks(s) + fused_y_blocks(s)) * 4;
+  const int nchunks = (s.world * s.tokens_per_slot + FUSED_CHUNK - 1) / FUSED_CHUNK;
+  return (size_t)(C_WORDS + fused_h_blocks(s) + fused_y_blocks(s) + nchunks) * 4;
 }
 
 cudaError_t launch_fused(const sym_heap &h, const float *logits, const uint16_t *x,
@@ -739,6 +869,10 @@ cudaError_t launch_fused(const sym_heap &h, const float *logits, const uint16_t 
                     FUSED_THREADS / 32 * SCATTER_SLOTS_MAX * 32 * sizeof(void *) <= (size_t)XCH_BYTES,
                 "per-warp tables live in the exchange buffer");
   static_assert(256 + FUSED_THREADS / 32 * SCATTER_SLOTS_MAX * 8 <= FUSED_CTRL_SMEM, "scatter barriers");
+  static_assert(2 * 8 * 3 * 32 * 16 <= STAGES * STAGE_BYTES / (FUSED_THREADS / 32) &&
+                    2 * 4 * 6 * 32 * 16 <= STAGES * STAGE_BYTES / (FUSED_THREADS / 32) &&
+                    2 * 2 * 8 * 32 * 16 <= STAGES * STAGE_BYTES / (FUSED_THREADS / 32),
+                "combine stream buffers fit a warp's share of the ring");
   const size_t smem = 1024 + (size_t)STAGES * STAGE_BYTES + XCH_BYTES + FUSED_CTRL_SMEM +
                       tok_tables_bytes(E);
   cudaError_t err = cudaFuncSetAttribute(moe_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -68,8 +68,9 @@ def test_heap_layout(name):
             (d.off_cnt, e_loc * 4), (d.off_recv_off, e_loc * 4), (d.off_total, 4),
             (d.off_status, 4), (d.off_ready, d.num_ready * 4),
             (d.off_hist, cfg["num_experts"] * ((n + 31) // 32) * 4),
-            # control words + one h and one y readiness counter per 256-row token tile
-            (d.off_ctrl, 4 * (64 + 2 * (n * k // 256 + cfg["num_experts"] + 1)))]
+            # control words + one h and one y readiness counter per 256-row token
+            # tile + a route-task counter per 32-token chunk
+            (d.off_ctrl, 4 * (64 + 2 * (n * k // 256 + cfg["num_experts"] + 1) + (n + 31) // 32))]
     for (o, b), (o2, _) in zip(wins, wins[1:]):
         assert o % 1024 == 0 and o + b <= o2
     assert wins[-1][0] + wins[-1][1] <= prs
