@@ -11,10 +11,11 @@
 //            per warp when there are fewer chunks than CTAs (logits rows
 //            staged in shared memory); the CTA that finishes the last route
 //            task of a 32-token chunk counts the chunk (per-expert bitmasks give
-//            every pair its rank in the chunk and the chunk histogram).  The
-//            CTA that counts the last chunk runs the scan (counts, receive
-//            offsets, totals) and clears the readiness counters, then
-//            publishes scan_done = epoch.
+//            every pair its rank in the chunk and the chunk histogram).  Once
+//            every chunk is counted, CTAs take per-expert scan tasks (prefix
+//            over the chunks, expert counts); the CTA completing the last one
+//            computes receive offsets and totals, clears the readiness
+//            counters and publishes scan_done = epoch.
 //   phase 2  scatter, one warp per token: rows go straight into the
 //            destination slot's recv_x window; each row raises the ready
 //            counter of its 128-row block (release).
@@ -58,9 +59,11 @@ enum Ctl : int {
   C_SCAN_DONE = 2,  // epoch of the last completed scan
   C_SCATTER_NEXT = 3,
   C_SCATTER_DONE = 4,  // scatter tasks completed (pos final for the combine)
+  C_SCAN_NEXT = 5,     // per-expert scan tasks claimed
   C_COMB_NEXT = 6,
   C_EXIT = 7,
   C_ABORT = 8,
+  C_SCAN_TASKS = 9,  // per-expert scan tasks completed
   C_WORDS = 64
 };
 
@@ -207,39 +210,58 @@ __device__ inline void count_chunk(const sym_heap &h, const FusedArgs &a, int ch
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)e * nchunks + chunk] = __popc(mask[e]);
 }
 
-// The scan, run by the CTA that completed the last chunk.
-__device__ inline void scan_and_publish(const sym_heap &h, int32_t *cnt_s) {
+// Scan task: one expert's chunk histogram row, split into 8 contiguous
+// segments (one per warp): exclusive prefix over the chunks in place and the
+// expert's row count into its slot's cnt window.  seg_s: 8 ints.
+__device__ inline void scan_expert(const sym_heap &h, int e, int *seg_s) {
   const int E = h.s.num_experts, W = h.s.world, E_loc = E / W;
   const int N = W * h.s.tokens_per_slot;
   const int nchunks = (N + FUSED_CHUNK - 1) / FUSED_CHUNK;
-  int32_t *hist = win<int32_t>(h, 0, h.off_hist);
   const int lane = lane_id(), wid = warp_id(), nw = blockDim.x >> 5;
-  __threadfence();
-  for (int e = wid; e < E; e += nw) {
-    int32_t *row = hist + (size_t)e * nchunks;
-    int carry = 0;
-    for (int c0 = 0; c0 < nchunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int v = c < nchunks ? __ldcg(row + c) : 0;
-      int incl = v;
+  int32_t *row = win<int32_t>(h, 0, h.off_hist) + (size_t)e * nchunks;
+  const int seg = (nchunks + nw - 1) / nw;
+  const int c_begin = min(nchunks, wid * seg), c_end = min(nchunks, c_begin + seg);
+  int total = 0;  // pass 1: this segment's sum
+  for (int c = c_begin + lane; c < c_end; c += 32) total += __ldcg(row + c);
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-      }
-      if (c < nchunks) row[c] = carry + incl - v;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) cnt_s[e] = carry;
-  }
+  for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
+  if (lane == 0) seg_s[wid] = total;
   __syncthreads();
+  int carry = 0;
+  for (int w = 0; w < wid; ++w) carry += seg_s[w];
+  for (int c0 = c_begin; c0 < c_end; c0 += 32) {  // pass 2: exclusive prefix in place
+    const int c = c0 + lane;
+    const int v = c < c_end ? __ldcg(row + c) : 0;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (c < c_end) row[c] = carry + incl - v;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (threadIdx.x == 0) {
+    int all = 0;
+    for (int w = 0; w < nw; ++w) all += seg_s[w];
+    win<int32_t>(h, e / E_loc, h.off_cnt)[e % E_loc] = all;
+  }
+  __syncthreads();  // seg_s is reused by the next task
+}
+
+// After the last scan task: receive offsets and totals per slot, clear the
+// readiness counters of this launch, publish scan_done = epoch.
+__device__ inline void finish_scan(const sym_heap &h) {
+  const int E = h.s.num_experts, W = h.s.world, E_loc = E / W;
+  const int N = W * h.s.tokens_per_slot;
+  const int nchunks = (N + FUSED_CHUNK - 1) / FUSED_CHUNK;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int d = e / E_loc, l = e % E_loc;
+    const int32_t *cnt = win<const int32_t>(h, d, h.off_cnt);
     int off = 0;
-    for (int i = 0; i < l; ++i) off += cnt_s[d * E_loc + i];
-    win<int32_t>(h, d, h.off_cnt)[l] = cnt_s[e];
+    for (int i = 0; i < l; ++i) off += __ldcg(cnt + i);
     win<int32_t>(h, d, h.off_recv_off)[l] = off;
-    if (l == E_loc - 1) *win<int32_t>(h, d, h.off_total) = off + cnt_s[e];
+    if (l == E_loc - 1) *win<int32_t>(h, d, h.off_total) = off + __ldcg(cnt + l);
   }
   for (int i = threadIdx.x; i < W * (int)h.num_ready; i += blockDim.x)
     win<uint32_t>(h, i / h.num_ready, h.off_ready)[i % h.num_ready] = 0u;
@@ -623,11 +645,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
   tc_fence_after();
   p.tmem_base = *tmem_base_s;
 
-  // ---------------- phase 1: route + count (the last finisher scans)
+  // ---------------- phase 1: route, count, scan
   // Route tasks of rt tokens: a whole 32-token chunk when there are chunks
   // for every CTA, else one token per warp (short batches).  The CTA finishing
-  // the last route task of a chunk counts that chunk; the CTA counting the
-  // last chunk scans.
+  // the last route task of a chunk counts that chunk.
   {
     const int rt = nchunks >= (int)gridDim.x ? FUSED_CHUNK : ROUTE_TOKENS;
     const int nroute = (N + rt - 1) / rt;
@@ -649,9 +670,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
       count_chunk(h, a, c, reinterpret_cast<uint32_t *>(ring) + (FUSED_THREADS / 32) * h.s.num_experts);
       __threadfence();
       __syncthreads();
-      if (threadIdx.x == 0) *bcast = (int)atomicAdd(ctl(h) + C_ROUTE_DONE, 1u);
+      if (threadIdx.x == 0) atomicAdd(ctl(h) + C_ROUTE_DONE, 1u);
+    }
+  }
+  // Scan tasks, one per expert, once every chunk is counted (all route tasks
+  // are claimed by running CTAs, so the wait ends); the CTA completing the
+  // last scan task finishes the scan.
+  if (threadIdx.x == 0) *bcast = wait_geq(h, ctl(h) + C_ROUTE_DONE, (uint32_t)nchunks) ? 1 : 0;
+  __syncthreads();
+  if (*bcast) {
+    int *seg_s = reinterpret_cast<int *>(ring);
+    for (;;) {
+      const int e = claim(h, C_SCAN_NEXT, bcast);
+      if (e >= h.s.num_experts) break;
+      scan_expert(h, e, seg_s);
+      __threadfence();
       __syncthreads();
-      if (*bcast == nchunks - 1) scan_and_publish(h, reinterpret_cast<int32_t *>(ring));
+      if (threadIdx.x == 0) *bcast = (int)atomicAdd(ctl(h) + C_SCAN_TASKS, 1u);
+      __syncthreads();
+      if (*bcast == h.s.num_experts - 1) {
+        __threadfence();  // acquire every scan task's counts
+        finish_scan(h);
+      }
     }
   }
 
@@ -839,6 +879,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
       uint32_t *c = ctl(h);
       c[C_ROUTE_NEXT] = 0;
       c[C_ROUTE_DONE] = 0;
+      c[C_SCAN_NEXT] = 0;
+      c[C_SCAN_TASKS] = 0;
       c[C_SCATTER_NEXT] = 0;
       c[C_SCATTER_DONE] = 0;
       c[C_COMB_NEXT] = 0;
