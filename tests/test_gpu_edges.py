@@ -27,7 +27,7 @@ def _oracle_from_idx(cfg, idx, w, wfn):
     rx = oracle.dispatch_rows(ms.x_np(cfg), rp, k)
     h, y, ye = oracle.expert_ffn(rx, cnt, off, E, W, wfn)
     out = oracle.combine(y, idx, w, pos, E, W)
-    return dict(cnt=cnt, off=off, tot=tot, pos=pos, y=y, y_exact=ye, out=out)
+    return dict(cnt=cnt, off=off, tot=tot, pos=pos, rx=rx, y=y, y_exact=ye, out=out)
 
 
 def _run(sm, cfg, idx_np, w_np, fused):
@@ -136,3 +136,20 @@ def test_remainder_rows_on_last_tile(sm, fused):
         t = int(ref["tot"][d])
         assert_close(bits(heap.y(d)[:t]), ref["y_exact"][d], f"slot {d} y")
     assert_close(bits(out), bf16_f64(ref["out"]), "remainder tiles out")
+
+
+@pytest.mark.parametrize("fused", [0, 1])
+def test_wide_rows(sm, fused):
+    """H = 16384: the staged scatter moves a row in two register passes and the
+    fused scatter's rows no longer fit a warp's share of the ring (plain-copy
+    path); the combine streams a row in many passes."""
+    cfg = dict(world=2, tokens_per_slot=24, hidden=16384, num_experts=4, topk=2, inter=128)
+    lg = ms.logits_np(cfg)
+    idx, w = oracle.route_topk(lg, cfg["topk"])
+    heap, out, w_used = _run(sm, cfg, idx, w, fused)
+    assert heap.status() == 0
+    ref = _oracle_from_idx(cfg, idx, w_used, fresh_weight_fn(cfg, DEV))
+    for d in range(cfg["world"]):
+        t = int(ref["tot"][d])
+        assert np.array_equal(bits(heap.recv_x(d)[:t]), ref["rx"][d])   # dispatched rows, bit-exact
+    assert_close(bits(out), bf16_f64(ref["out"]), "H=16384 out")
