@@ -26,6 +26,8 @@ from .moe import (  # noqa: F401
     expert_ffn_rows,
     expert_ffn,
     combine,
+    scale_rows,
+    combine_sum,
     pipeline,
     slot_address,
 )

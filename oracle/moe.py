@@ -214,14 +214,47 @@ def combine(y_bits: list, idx: np.ndarray, w: np.ndarray, pos: np.ndarray,
 
 
 # ---------------------------------------------------------------------------
+# variant: routing weights applied in the expert epilogue
+# ---------------------------------------------------------------------------
+# The pages apply the weights where combine takes them.  The variant moves
+# them to the receiving side: each received row's expert output is scaled by
+# the weight of its (token, k) pair (recv_w, written by the dispatch) before
+# the output is rounded, and the combine only sums.
+
+def scale_rows(y_exact: list, recv_w: list) -> list:
+    """y_w[d][p] = bf16(recv_w[d][p] * y[d][p]) with y before its rounding:
+    one rounding of the weighted expert output."""
+    return [round_f64_to_bf16_bits(np.asarray(ye, dtype=np.float64) *
+                                   np.asarray(rw, dtype=np.float64)[:, None])
+            for ye, rw in zip(y_exact, recv_w)]
+
+
+def combine_sum(y_bits: list, idx: np.ndarray, pos: np.ndarray, num_experts: int,
+                world: int) -> np.ndarray:
+    """out[g] = bf16(sum_j y[slot of idx[g, j]][pos[g, j]]), j ascending: the
+    combine of rows that already carry their weights."""
+    idx = np.asarray(idx)
+    n, k = idx.shape
+    e_loc = num_experts // world
+    acc = np.zeros((n, y_bits[0].shape[1]), dtype=np.float64)
+    for j in range(k):
+        for g in range(n):
+            d = int(idx[g, j]) // e_loc
+            acc[g] += bf16_bits_to_f64(y_bits[d][int(pos[g, j])])
+    return round_f64_to_bf16_bits(acc)
+
+
+# ---------------------------------------------------------------------------
 # whole path
 # ---------------------------------------------------------------------------
 
-def pipeline(logits, x_bits, shape: dict, weight_fn):
+def pipeline(logits, x_bits, shape: dict, weight_fn, weights_in_ffn: bool = False):
     """route -> count/place -> dispatch rows -> expert FFN -> combine.
 
     ``shape`` has world, num_experts, topk; ``weight_fn(e)`` gives expert e's
-    (Wg, Wu, Wd) bf16 bits.  Returns a dict with every intermediate.
+    (Wg, Wu, Wd) bf16 bits.  ``weights_in_ffn``: the variant above (y holds
+    the weighted rows, the combine sums).  Returns a dict with every
+    intermediate.
     """
     world, num_experts, k = shape["world"], shape["num_experts"], shape["topk"]
     idx, w = route_topk(logits, k)
@@ -229,7 +262,11 @@ def pipeline(logits, x_bits, shape: dict, weight_fn):
     pos, recv_pair, recv_w = place_pairs(idx, w, num_experts, world)
     recv_x = dispatch_rows(x_bits, recv_pair, k)
     h, y, y_exact = expert_ffn(recv_x, cnt, recv_off, num_experts, world, weight_fn)
-    out = combine(y, idx, w, pos, num_experts, world)
+    if weights_in_ffn:
+        y = scale_rows(y_exact, recv_w)
+        out = combine_sum(y, idx, pos, num_experts, world)
+    else:
+        out = combine(y, idx, w, pos, num_experts, world)
     return dict(idx=idx, w=w, cnt=cnt, recv_off=recv_off, total_recv=total_recv,
                 pos=pos, recv_pair=recv_pair, recv_w=recv_w, recv_x=recv_x,
                 h=h, y=y, y_exact=y_exact, out=out)

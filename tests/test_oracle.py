@@ -277,3 +277,52 @@ def test_pipeline_tiny_consistency():
             _, yb, _ = oracle.expert_ffn_rows(ms.x_np(cfg, rows=[g]), *wts)
             acc += float(res["w"][g, j]) * oracle.bf16_bits_to_f64(yb[0])
         assert np.array_equal(res["out"][g], oracle.round_f64_to_bf16_bits(acc))
+
+
+# ------------------------------------------ variant: weights in the expert epilogue
+
+def test_scale_rows_rounds_once():
+    # 3 * (1 + 3*2^-9) = 3.017578125 -> bf16 3.015625.  Weighting the already
+    # rounded y (1.0078125) instead would give 3.0234375 -> 3.03125 (tie to even).
+    ye = [np.array([[1.0 + 3 * 2.0 ** -9, -2.0]])]
+    yw = oracle.scale_rows(ye, [np.array([3.0], dtype=np.float32)])
+    assert oracle.bf16_bits_to_f64(yw[0]).tolist() == [[3.015625, -6.0]]
+    late = oracle.round_f64_to_bf16_bits(3.0 * oracle.bf16_bits_to_f64(oracle.round_f64_to_bf16_bits(ye[0])))
+    assert oracle.bf16_bits_to_f64(late)[0, 0] == 3.03125   # the mistake the pin excludes
+
+
+def test_combine_sum_is_combine_with_unit_weights():
+    rng = np.random.default_rng(11)
+    idx, w = _random_routing(30, 6, 3, 4)
+    pos, _, _ = oracle.place_pairs(idx, w, 6, 3)
+    _, _, tot = oracle.count_experts(idx, 6, 3)
+    y = [_bits(rng.standard_normal((int(tot[d]), 8))) for d in range(3)]
+    a = oracle.combine_sum(y, idx, pos, 6, 3)
+    b = oracle.combine(y, idx, np.ones_like(w), pos, 6, 3)
+    assert np.array_equal(a, b)
+    # brute force for one token
+    g = 7
+    acc = sum(oracle.bf16_bits_to_f64(y[int(idx[g, j]) // 2][pos[g, j]]) for j in range(3))
+    assert np.array_equal(a[g], oracle.round_f64_to_bf16_bits(acc))
+
+
+def test_weights_in_ffn_k1_equals_baseline():
+    # k = 1: every weight is exactly 1, so scaling and the plain sum change nothing
+    cfg = dict(ms.CONFIGS["tiny"], topk=1)
+    wfn = lambda e: tuple(ms.weight_np(cfg, n, e) for n in ("gate", "up", "down"))
+    a = oracle.pipeline(ms.logits_np(cfg), ms.x_np(cfg), cfg, wfn)
+    b = oracle.pipeline(ms.logits_np(cfg), ms.x_np(cfg), cfg, wfn, weights_in_ffn=True)
+    assert np.all(a["w"] == 1.0)
+    assert np.array_equal(a["out"], b["out"])
+    for d in range(cfg["world"]):
+        assert np.array_equal(a["y"][d], b["y"][d])
+
+
+def test_weights_in_ffn_exact_on_integer_ffn():
+    # integer expert outputs and power-of-two weights: w*y is exact in bf16, so
+    # weighting before or after the rounding and summing in the combine agree
+    a, wg, wu, wd, h_ref, y_ref = integer_ffn_case(6, 24, 40)
+    _, y, ye = oracle.expert_ffn_rows(a, wg, wu, wd)
+    w = np.array([0.5, 0.25, 2.0, 1.0, 0.125, 4.0], dtype=np.float32)
+    yw = oracle.scale_rows([ye], [w])[0]
+    assert np.array_equal(oracle.bf16_bits_to_f64(yw), y_ref * w[:, None])
