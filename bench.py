@@ -36,6 +36,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--config", default="mixtral")
     p.add_argument("--fused", action="store_true", help="single-launch pipeline")
+    p.add_argument("--weights-in-ffn", action="store_true",
+                   help="routing weights applied in the expert epilogue, unweighted combine")
     p.add_argument("--unfused", action="store_true",
                    help="stage-by-stage launches even for a workload defined as fused")
     p.add_argument("--tokens-per-slot", type=int, default=0,
@@ -79,13 +81,14 @@ def l2_statement(cfg: dict) -> str:
             "a small-case timing, not a roofline measurement")
 
 
-def workload_config(name: str, cfg: dict, fused: bool) -> dict:
+def workload_config(name: str, cfg: dict, fused: bool, weights_in_ffn: bool = False) -> dict:
     import moe_synth as ms
     n = cfg["world"] * cfg["tokens_per_slot"]
     return {"workload": ms.CONFIG_TITLES.get(name, name), "preset": name,
             "world_slots": cfg["world"], "tokens_per_slot": cfg["tokens_per_slot"],
             "tokens_per_step": n, "hidden": cfg["hidden"], "inter": cfg["inter"],
             "experts": cfg["num_experts"], "topk": cfg["topk"], "fused": bool(fused),
+            "weights_in_ffn": bool(weights_in_ffn),
             "l2": l2_statement(cfg),
             "parallelism": "replicas"}
 
@@ -199,7 +202,7 @@ def peaks():
 # CPU oracle (baseline and reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample_run(cfg: dict, tokens, weights: dict):
+def oracle_sample_run(cfg: dict, tokens, weights: dict, weights_in_ffn: bool = False):
     """Time the oracle, as it stands, over a sample of tokens: routing of the
     sample, placement of its pairs, the SwiGLU FFN of every received row, and
     the combine.  ``weights[e]`` are the experts' bf16 bits (inputs, not timed
@@ -212,7 +215,7 @@ def oracle_sample_run(cfg: dict, tokens, weights: dict):
     t0 = time.perf_counter()
     sample = dict(cfg, tokens_per_slot=len(tokens), world=1, num_experts=cfg["num_experts"])
     res = oracle.pipeline(lg, xs, dict(world=1, num_experts=cfg["num_experts"], topk=cfg["topk"]),
-                          lambda e: weights[e])
+                          lambda e: weights[e], weights_in_ffn=weights_in_ffn)
     dt = time.perf_counter() - t0
     assert res["out"].shape == (len(tokens), cfg["hidden"])
     del sample
@@ -271,7 +274,7 @@ def run_reference(args):
     for s in range(args.warmup + args.steps):
         tokens = np.sort(rng.choice(n, size=per_step, replace=False))
         wts.update(sample_weights(cfg, tokens, dev, skip=set(wts)))
-        dt = oracle_sample_run(cfg, tokens, wts)
+        dt = oracle_sample_run(cfg, tokens, wts, bool(getattr(args, "weights_in_ffn", False)))
         if s >= args.warmup:
             times.append(dt)
     tot = sum(times)
@@ -280,7 +283,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(args.config, cfg, args.fused),
+        "data": "synthetic", "config": workload_config(args.config, cfg, args.fused, getattr(args, "weights_in_ffn", False)),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
                          "sample": f"{per_step} random tokens of the workload per step (their "
                                    f"routing, placement, expert FFN rows and combine); expert "
@@ -308,6 +311,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     cfg = get_cfg(args)
     fused = 1 if (args.fused or (cfg.get("fused") and not args.unfused)) else 0
+    wif = bool(getattr(args, "weights_in_ffn", False))
     n, k, H = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"], cfg["hidden"]
 
     heap = sm.SymHeap(cfg, dev)
@@ -333,13 +337,13 @@ def run_ours(args):
 
     def step(i=None):
         if fused:
-            heap.pipeline(logits, x, wg, wu, wd, idx, w, out, fused=1, stream=stream)
+            heap.pipeline(logits, x, wg, wu, wd, idx, w, out, fused=1, weights_in_ffn=wif, stream=stream)
             return
         ev = stage_evs[i] if i is not None else None
         calls = [lambda: heap.route_topk(logits, idx, w, stream=stream),
                  lambda: heap.dispatch(x, idx, w, stream=stream),
-                 lambda: heap.expert_ffn(wg, wu, wd, stream=stream),
-                 lambda: heap.combine(idx, w, out, stream=stream)]
+                 lambda: heap.expert_ffn(wg, wu, wd, weighted_rows=wif, stream=stream),
+                 lambda: heap.combine(idx, w, out, unweighted=wif, stream=stream)]
         for j, call in enumerate(calls):
             if ev:
                 ev[j].record(stream)
@@ -455,7 +459,8 @@ def run_ours(args):
                 stream.wait_event(up)
                 if downloaded[b] is not None:
                     stream.wait_event(downloaded[b])
-                heap.pipeline(lg_d[b], x_d[b], wg, wu, wd, idx, w, out_d[b], fused=fused, stream=stream)
+                heap.pipeline(lg_d[b], x_d[b], wg, wu, wd, idx, w, out_d[b], fused=fused, weights_in_ffn=wif,
+                              stream=stream)
                 computed[b] = ev()
                 computed[b].record(stream)
                 with torch.cuda.stream(s_down):
@@ -488,7 +493,7 @@ def run_ours(args):
         ntok = int(os.environ.get("SYMMOE_CPU_TOKENS", "64"))
         tokens = np.sort(np.random.default_rng(0).choice(n, size=ntok, replace=False))
         wts = sample_weights(cfg, tokens, dev)
-        dt = oracle_sample_run(cfg, tokens, wts)
+        dt = oracle_sample_run(cfg, tokens, wts, wif)
         cpu = {"value": ntok / dt, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
                "sample": f"{ntok} random tokens of the workload (routing, placement, all "
                          f"{ntok * k} expert FFN rows, combine) in {dt:.1f} s; fp64 numpy"}
@@ -498,7 +503,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(args.config, cfg, fused),
+            "config": workload_config(args.config, cfg, fused, wif),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),

@@ -83,7 +83,9 @@ def lib() -> ctypes.CDLL:
         L.moe_route_topk.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
         L.moe_dispatch.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
         L.moe_expert_ffn.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
+        L.moe_expert_ffn_ex.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, ctypes.c_int, _vp]
         L.moe_combine.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp, _vp]
+        L.moe_combine_ex.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp, ctypes.c_int, _vp]
         L.moe_combine_fallback_copies.restype = _u64
         L.moe_pipeline.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                    ctypes.c_int, _vp]
@@ -169,15 +171,33 @@ def moe_combine(heap: SymHeapDesc, expert_out, idx, w, out, stream=None) -> None
                              _stream(stream)), "moe_combine")
 
 
+# flags of the _ex calls and pipeline modes (include/symmoe.h)
+SYM_FFN_WEIGHTED_ROWS = 1
+SYM_COMBINE_UNWEIGHTED = 1
+SYM_PIPE_FUSED = 1
+SYM_PIPE_WEIGHTS_IN_FFN = 2
+
+
+def moe_expert_ffn_ex(heap: SymHeapDesc, w_gate, w_up, w_down, flags: int = 0, stream=None) -> None:
+    _check(lib().moe_expert_ffn_ex(ctypes.byref(heap), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                                   int(flags), _stream(stream)), "moe_expert_ffn_ex")
+
+
+def moe_combine_ex(heap: SymHeapDesc, expert_out, idx, w, out, flags: int = 0, stream=None) -> None:
+    _check(lib().moe_combine_ex(ctypes.byref(heap), _ptr(expert_out), _ptr(idx), _ptr(w), _ptr(out),
+                                int(flags), _stream(stream)), "moe_combine_ex")
+
+
 def moe_combine_fallback_copies() -> int:
     return int(lib().moe_combine_fallback_copies())
 
 
 def moe_pipeline(heap: SymHeapDesc, logits, x, w_gate, w_up, w_down, idx, w, out,
-                 fused: int = 0, stream=None) -> None:
+                 mode: int = 0, stream=None) -> None:
+    """mode: SYM_PIPE_FUSED and/or SYM_PIPE_WEIGHTS_IN_FFN bits (0: staged)."""
     _check(lib().moe_pipeline(ctypes.byref(heap), _ptr(logits), _ptr(x), _ptr(w_gate),
                               _ptr(w_up), _ptr(w_down), _ptr(idx), _ptr(w), _ptr(out),
-                              int(fused), _stream(stream)), "moe_pipeline")
+                              int(mode), _stream(stream)), "moe_pipeline")
 
 
 def moe_dispatch_layout_noalloc(shape, idx, cnt, recv_off, total_recv, pos, stream=None) -> None:
@@ -277,14 +297,16 @@ class SymHeap:
     def dispatch(self, x, idx, w, stream=None):
         moe_dispatch(self.desc, x, idx, w, stream)
 
-    def expert_ffn(self, wg, wu, wd, stream=None):
-        moe_expert_ffn(self.desc, wg, wu, wd, stream)
+    def expert_ffn(self, wg, wu, wd, weighted_rows=False, stream=None):
+        moe_expert_ffn_ex(self.desc, wg, wu, wd, SYM_FFN_WEIGHTED_ROWS if weighted_rows else 0, stream)
 
-    def combine(self, idx, w, out, expert_out=None, stream=None):
-        moe_combine(self.desc, expert_out, idx, w, out, stream)
+    def combine(self, idx, w, out, expert_out=None, unweighted=False, stream=None):
+        moe_combine_ex(self.desc, expert_out, idx, w, out, SYM_COMBINE_UNWEIGHTED if unweighted else 0,
+                       stream)
 
-    def pipeline(self, logits, x, wg, wu, wd, idx, w, out, fused=0, stream=None):
-        moe_pipeline(self.desc, logits, x, wg, wu, wd, idx, w, out, fused, stream)
+    def pipeline(self, logits, x, wg, wu, wd, idx, w, out, fused=0, weights_in_ffn=False, stream=None):
+        mode = (SYM_PIPE_FUSED if fused else 0) | (SYM_PIPE_WEIGHTS_IN_FFN if weights_in_ffn else 0)
+        moe_pipeline(self.desc, logits, x, wg, wu, wd, idx, w, out, mode, stream)
 
 
 lib()  # fail loudly at import if the CUDA library is missing

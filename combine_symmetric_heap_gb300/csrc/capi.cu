@@ -18,13 +18,15 @@ cudaError_t launch_route_topk(const sym_heap &h, const float *logits, int32_t *i
 cudaError_t launch_dispatch(const sym_heap &h, const uint16_t *x, const int32_t *idx,
                             const float *w, cudaStream_t st);
 cudaError_t launch_expert_ffn(const sym_heap &h, const uint16_t *wg, const uint16_t *wu,
-                              const uint16_t *wd, int num_sms, int wait_ready, cudaStream_t st);
+                              const uint16_t *wd, int num_sms, int wait_ready, int scale_rows,
+                              cudaStream_t st);
 cudaError_t launch_combine(const sym_heap &h, const uint16_t *expert_out, const int32_t *idx,
-                           const float *w, uint16_t *out, int num_sms, cudaStream_t st);
+                           const float *w, uint16_t *out, int unit_weights, int num_sms, cudaStream_t st);
 size_t fused_ctrl_bytes(const moe_shape &s);
 cudaError_t launch_fused(const sym_heap &h, const float *logits, const uint16_t *x,
                          const uint16_t *wg, const uint16_t *wu, const uint16_t *wd,
-                         int32_t *idx, float *w, uint16_t *out, int num_sms, cudaStream_t st);
+                         int32_t *idx, float *w, uint16_t *out, int weights_in_ffn, int num_sms,
+                         cudaStream_t st);
 }  // namespace symmoe
 
 using namespace symmoe;
@@ -183,18 +185,28 @@ int moe_dispatch(sym_heap *h, const uint16_t *x, const int32_t *idx, const float
   return from_cuda(launch_dispatch(*h, x, idx, w, (cudaStream_t)stream));
 }
 
-int moe_expert_ffn(const sym_heap *h, const uint16_t *w_gate, const uint16_t *w_up,
-                   const uint16_t *w_down, symmoe_stream_t stream) {
-  if (!heap_ok(h) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down))
+int moe_expert_ffn_ex(const sym_heap *h, const uint16_t *w_gate, const uint16_t *w_up,
+                      const uint16_t *w_down, int flags, symmoe_stream_t stream) {
+  if (!heap_ok(h) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+      (flags & ~SYM_FFN_WEIGHTED_ROWS))
     return SYM_EINVAL;
   const int sms = num_sms_of_current_device();
   if (sms <= 0) return SYM_ECUDA;
-  return from_cuda(launch_expert_ffn(*h, w_gate, w_up, w_down, sms, 1, (cudaStream_t)stream));
+  return from_cuda(launch_expert_ffn(*h, w_gate, w_up, w_down, sms, 1, (flags & SYM_FFN_WEIGHTED_ROWS) ? 1 : 0,
+                                     (cudaStream_t)stream));
 }
 
-int moe_combine(const sym_heap *h, const uint16_t *expert_out, const int32_t *idx,
-                const float *w, uint16_t *out, symmoe_stream_t stream) {
-  if (!heap_ok(h) || !aligned4(idx) || !aligned4(w) || !aligned16(out)) return SYM_EINVAL;
+int moe_expert_ffn(const sym_heap *h, const uint16_t *w_gate, const uint16_t *w_up,
+                   const uint16_t *w_down, symmoe_stream_t stream) {
+  return moe_expert_ffn_ex(h, w_gate, w_up, w_down, 0, stream);
+}
+
+int moe_combine_ex(const sym_heap *h, const uint16_t *expert_out, const int32_t *idx,
+                   const float *w, uint16_t *out, int flags, symmoe_stream_t stream) {
+  const bool unit = (flags & SYM_COMBINE_UNWEIGHTED) != 0;
+  if (!heap_ok(h) || !aligned4(idx) || (!unit && !aligned4(w)) || !aligned16(out) ||
+      (flags & ~SYM_COMBINE_UNWEIGHTED))
+    return SYM_EINVAL;
   const uint16_t *view = reinterpret_cast<const uint16_t *>(h->base + h->off_y);
   const uint16_t *stage = nullptr;
   if (expert_out && expert_out != view) {
@@ -204,27 +216,34 @@ int moe_combine(const sym_heap *h, const uint16_t *expert_out, const int32_t *id
   }
   const int sms = num_sms_of_current_device();
   if (sms <= 0) return SYM_ECUDA;
-  return from_cuda(launch_combine(*h, stage, idx, w, out, sms, (cudaStream_t)stream));
+  return from_cuda(launch_combine(*h, stage, idx, w, out, unit ? 1 : 0, sms, (cudaStream_t)stream));
+}
+
+int moe_combine(const sym_heap *h, const uint16_t *expert_out, const int32_t *idx,
+                const float *w, uint16_t *out, symmoe_stream_t stream) {
+  return moe_combine_ex(h, expert_out, idx, w, out, 0, stream);
 }
 
 uint64_t moe_combine_fallback_copies(void) { return g_fallback_copies.load(); }
 
 int moe_pipeline(sym_heap *h, const float *logits, const uint16_t *x, const uint16_t *w_gate,
                  const uint16_t *w_up, const uint16_t *w_down, int32_t *idx, float *w,
-                 uint16_t *out, int fused, symmoe_stream_t stream) {
+                 uint16_t *out, int mode, symmoe_stream_t stream) {
   if (!heap_ok(h) || !aligned4(logits) || !aligned16(x) || !aligned16(w_gate) ||
       !aligned16(w_up) || !aligned16(w_down) || !aligned4(idx) || !aligned4(w) ||
-      !aligned16(out) || (fused != 0 && fused != 1))
+      !aligned16(out) || (mode & ~(SYM_PIPE_FUSED | SYM_PIPE_WEIGHTS_IN_FFN)))
     return SYM_EINVAL;
   const cudaStream_t st = (cudaStream_t)stream;
   const int sms = num_sms_of_current_device();
   if (sms <= 0) return SYM_ECUDA;
+  const int weighted = (mode & SYM_PIPE_WEIGHTS_IN_FFN) ? 1 : 0;
   h->epoch += 1;
-  if (fused) return from_cuda(launch_fused(*h, logits, x, w_gate, w_up, w_down, idx, w, out, sms, st));
+  if (mode & SYM_PIPE_FUSED)
+    return from_cuda(launch_fused(*h, logits, x, w_gate, w_up, w_down, idx, w, out, weighted, sms, st));
   cudaError_t e = launch_route_topk(*h, logits, idx, w, st);
   if (e == cudaSuccess) e = launch_dispatch(*h, x, idx, w, st);
-  if (e == cudaSuccess) e = launch_expert_ffn(*h, w_gate, w_up, w_down, sms, 1, st);
-  if (e == cudaSuccess) e = launch_combine(*h, nullptr, idx, w, out, sms, st);
+  if (e == cudaSuccess) e = launch_expert_ffn(*h, w_gate, w_up, w_down, sms, 1, weighted, st);
+  if (e == cudaSuccess) e = launch_combine(*h, nullptr, idx, w, out, weighted, sms, st);
   return from_cuda(e);
 }
 

@@ -20,7 +20,7 @@ constexpr int COMBINE_THREADS = 128;
 template <int G>
 __global__ void __launch_bounds__(COMBINE_THREADS)
     combine_kernel(sym_heap h, const int32_t *__restrict__ idx, const float *__restrict__ w,
-                   uint4 *__restrict__ out) {
+                   uint4 *__restrict__ out, int unit_weights) {
   __shared__ const uint4 *src_s[32];
   __shared__ float w_s[32];
   const int E = h.s.num_experts, k = h.s.topk, T = h.s.tokens_per_slot, H = h.s.hidden;
@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
     if (e >= 0 && e < E && p >= 0 && (uint64_t)p < h.cap)
       src = win<const uint4>(h, e / E_loc, h.off_y) + (size_t)p * nvec;
     src_s[tid] = src;
-    w_s[tid] = w[(size_t)g * k + tid];
+    w_s[tid] = unit_weights ? 1.f : w[(size_t)g * k + tid];  // 1: rows already weighted
   }
   __syncthreads();
   uint4 *dst = out + (size_t)g * nvec;
@@ -107,16 +107,16 @@ __global__ void __launch_bounds__(256)
 }
 
 cudaError_t launch_combine(const sym_heap &h, const uint16_t *expert_out, const int32_t *idx,
-                           const float *w, uint16_t *out, int num_sms, cudaStream_t st) {
+                           const float *w, uint16_t *out, int unit_weights, int num_sms, cudaStream_t st) {
   const int N = h.s.world * h.s.tokens_per_slot;
   if (expert_out) {
     dim3 grid(num_sms * 2, h.s.world);
     stage_expert_out_kernel<<<grid, 256, 0, st>>>(h, reinterpret_cast<const uint4 *>(expert_out));
   }
   if (h.s.topk <= 2)
-    combine_kernel<2><<<N, COMBINE_THREADS, 0, st>>>(h, idx, w, reinterpret_cast<uint4 *>(out));
+    combine_kernel<2><<<N, COMBINE_THREADS, 0, st>>>(h, idx, w, reinterpret_cast<uint4 *>(out), unit_weights);
   else
-    combine_kernel<4><<<N, COMBINE_THREADS, 0, st>>>(h, idx, w, reinterpret_cast<uint4 *>(out));
+    combine_kernel<4><<<N, COMBINE_THREADS, 0, st>>>(h, idx, w, reinterpret_cast<uint4 *>(out), unit_weights);
   return cudaGetLastError();
 }
 

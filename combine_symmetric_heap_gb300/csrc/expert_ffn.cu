@@ -43,7 +43,7 @@ template <int KIND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     expert_gemm2_kernel(const sym_heap h, const __grid_constant__ CUtensorMap tm_a0,
                         const __grid_constant__ CUtensorMap tm_a1,
-                        const __grid_constant__ gemm2::BMaps tm_b, int wait_ready) {
+                        const __grid_constant__ gemm2::BMaps tm_b, int wait_ready, int scale_rows) {
   using namespace gemm2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -70,6 +70,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   p.abort = abort_flag;
   p.stop = stop_tile;
   p.tmo = h.wait_timeout_us;
+  p.scale_rows = scale_rows;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -255,7 +256,8 @@ int max_resident_pairs(const void *kern, int threads, size_t smem, int num_sms) 
 }
 
 cudaError_t launch_expert_ffn(const sym_heap &h, const uint16_t *wg, const uint16_t *wu,
-                              const uint16_t *wd, int num_sms, int wait_ready, cudaStream_t st) {
+                              const uint16_t *wd, int num_sms, int wait_ready, int scale_rows,
+                              cudaStream_t st) {
   using namespace gemm2;
   const int E = h.s.num_experts, H = h.s.hidden, I = h.s.inter;
   const size_t smem = gemm2_smem_bytes(E);
@@ -271,7 +273,7 @@ cudaError_t launch_expert_ffn(const sym_heap &h, const uint16_t *wg, const uint1
     if (err != cudaSuccess) return err;
     const int grid = 2 * max_resident_pairs((const void *)kern, GEMM_THREADS, smem, num_sms);
     if (grid <= 0) return cudaErrorInvalidConfiguration;
-    kern<<<grid, GEMM_THREADS, smem, st>>>(h, ta0, ta1, tb, wait_ready);
+    kern<<<grid, GEMM_THREADS, smem, st>>>(h, ta0, ta1, tb, wait_ready, 0);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   // GEMM2: A = 128 down rows of expert e per CTA ([E*H][I]), B = h token rows
@@ -283,7 +285,7 @@ cudaError_t launch_expert_ffn(const sym_heap &h, const uint16_t *wg, const uint1
     if (err != cudaSuccess) return err;
     const int grid = 2 * max_resident_pairs((const void *)kern, GEMM_THREADS, smem, num_sms);
     if (grid <= 0) return cudaErrorInvalidConfiguration;
-    kern<<<grid, GEMM_THREADS, smem, st>>>(h, ta0, ta0, tb, 0);
+    kern<<<grid, GEMM_THREADS, smem, st>>>(h, ta0, ta0, tb, 0, scale_rows);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   return cudaSuccess;

@@ -79,6 +79,7 @@ struct FusedArgs {
   int32_t *idx;
   float *w;
   uint16_t *out;
+  int weights_in_ffn;  // weights applied to y rows in the down epilogue; the combine sums
 };
 
 __device__ __forceinline__ uint32_t *ctl(const sym_heap &h) { return win<uint32_t>(h, 0, h.off_ctrl); }
@@ -419,7 +420,7 @@ __device__ inline void combine_token(const sym_heap &h, const FusedArgs &a, cons
       src = win<const uint4>(h, e / E_loc, h.off_y) + (size_t)p * (H / 8);
     }
     src_s[lane] = src;
-    w_s[lane] = __ldcg(a.w + (size_t)g * k + lane);
+    w_s[lane] = a.weights_in_ffn ? 1.f : __ldcg(a.w + (size_t)g * k + lane);
   }
   if (!__all_sync(0xffffffffu, ok)) return;
   uint4 *dst = reinterpret_cast<uint4 *>(a.out) + (size_t)g * (H / 8);
@@ -497,7 +498,7 @@ __device__ inline void combine_token_stream(const sym_heap &h, const FusedArgs &
       src = win<const uint4>(h, e / E_loc, h.off_y) + (size_t)p * (H / 8);
     }
     src_s[lane] = src;
-    w_s[lane] = __ldcg(a.w + (size_t)g * k + lane);
+    w_s[lane] = a.weights_in_ffn ? 1.f : __ldcg(a.w + (size_t)g * k + lane);
   }
   if (!__all_sync(0xffffffffu, ok)) return;
   uint4 *dst = reinterpret_cast<uint4 *>(a.out) + (size_t)g * (H / 8);
@@ -610,6 +611,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
   p.abort = abort_s;
   p.stop = never_s;
   p.tmo = h.wait_timeout_us;
+  p.scale_rows = a.weights_in_ffn;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -898,7 +900,7 @@ size_t fused_ctrl_bytes(const moe_shape &s) {
 
 cudaError_t launch_fused(const sym_heap &h, const float *logits, const uint16_t *x,
                          const uint16_t *wg, const uint16_t *wu, const uint16_t *wd, int32_t *idx,
-                         float *w, uint16_t *out, int num_sms, cudaStream_t st) {
+                         float *w, uint16_t *out, int weights_in_ffn, int num_sms, cudaStream_t st) {
   using namespace gemm2;
   const int E = h.s.num_experts, H = h.s.hidden, I = h.s.inter;
   CUtensorMap tg, tu, td;
@@ -923,7 +925,7 @@ cudaError_t launch_fused(const sym_heap &h, const float *logits, const uint16_t 
   // every pair resident at once: phase 3 assigns tiles to pairs statically
   const int grid = 2 * max_resident_pairs((const void *)moe_fused_kernel, FUSED_THREADS, smem, num_sms);
   if (grid <= 0) return cudaErrorInvalidConfiguration;
-  const FusedArgs a{logits, x, idx, w, out};
+  const FusedArgs a{logits, x, idx, w, out, weights_in_ffn};
   moe_fused_kernel<<<grid, FUSED_THREADS, smem, st>>>(h, a, tg, tu, trx, td, th);
   return cudaGetLastError();
 }

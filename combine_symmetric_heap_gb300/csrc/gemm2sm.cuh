@@ -323,6 +323,7 @@ struct Pipe {
   volatile int *abort;        // this CTA gives up (timeout or dependency failure)
   const volatile int *stop;   // roles stop before tile index *stop
   uint32_t tmo;               // wait limit, microseconds
+  int scale_rows;             // DOWN: y row p = bf16(recv_w[p] * acc) (weights in the epilogue)
 };
 
 __device__ __forceinline__ void ring_advance(int &stage, uint32_t &phase) {
@@ -467,7 +468,7 @@ __device__ __forceinline__ void release_acc(const Pipe &p, uint64_t *bar, int la
 // Epilogue of token rows [row, row + nrows) whose accumulators start at TMEM
 // address tcol (this warp's lane quarter q); head() runs once the first
 // 32 columns have been read.
-template <int KIND, typename Head>
+template <int KIND, bool SCALE, typename Head>
 __device__ void epi_rows(const sym_heap &h, const Pipe &p, const TileInfo &ti, uint32_t tcol, int row,
                          int nrows, int q, int lane, Head head) {
   if (KIND == GATE_UP) {
@@ -506,14 +507,20 @@ __device__ void epi_rows(const sym_heap &h, const Pipe &p, const TileInfo &ti, u
     const int feature = ti.f * 256 + (int)p.rank * 128 + q * 32 + lane;
     uint16_t *out = win<uint16_t>(h, ti.d, h.off_y) + (size_t)row * ld + feature;
     const bool live = feature < ld;  // a last feature tile may run past H
+    const float *wrow = win<const float>(h, ti.d, h.off_recv_w) + row;  // SCALE: the rows' weights
     for (int c0 = 0; c0 < nrows; c0 += 32) {
+      float wl = 1.f;
+      if (SCALE && c0 + lane < nrows) wl = __ldcg(wrow + c0 + lane);
       uint32_t v[32];
       tmem_ld32(tcol + c0, v);
       tmem_ld_wait();
       if (c0 == 0) head();
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (live && c0 + c < nrows) out[(size_t)(c0 + c) * ld] = to_bf16(__uint_as_float(v[c]));
+      for (int c = 0; c < 32; ++c) {
+        float yv = __uint_as_float(v[c]);
+        if (SCALE) yv *= __shfl_sync(0xffffffffu, wl, c);
+        if (live && c0 + c < nrows) out[(size_t)(c0 + c) * ld] = to_bf16(yv);
+      }
     }
   }
 }
@@ -536,9 +543,13 @@ __device__ bool epi_tile(const sym_heap &h, const Pipe &p, EpiState &s, const Ti
   // remainder may go there), the whole main accumulator at the end.
   for (int part = ti.valid > BN ? 1 : 0; part >= 0; --part) {
     const int buf = part ? (b ^ 1) : b;
-    epi_rows<KIND>(h, p, ti, lanes + (uint32_t)(buf * ACC_COLS), ti.row0 + part * BN,
-                   part ? ti.valid - BN : min(ti.valid, BN), q, lane,
-                   [&]() { release_acc(p, &p.acc_head[buf], lane); });
+    const uint32_t tcol = lanes + (uint32_t)(buf * ACC_COLS);
+    const int row = ti.row0 + part * BN, nrows = part ? ti.valid - BN : min(ti.valid, BN);
+    auto head = [&]() { release_acc(p, &p.acc_head[buf], lane); };
+    if (KIND == DOWN && p.scale_rows)
+      epi_rows<KIND, true>(h, p, ti, tcol, row, nrows, q, lane, head);
+    else
+      epi_rows<KIND, false>(h, p, ti, tcol, row, nrows, q, lane, head);
     if (part == 0) release_acc(p, &p.acc_empty[buf], lane);
   }
   s.abuf = b ^ 1;

@@ -187,6 +187,20 @@ int moe_expert_ffn(const sym_heap *h, const uint16_t *w_gate, const uint16_t *w_
                    const uint16_t *w_down, symmoe_stream_t stream);
 
 /*
+ * moe_expert_ffn_ex: moe_expert_ffn with flags (0: identical to it).
+ *   SYM_FFN_WEIGHTED_ROWS: the routing weights move from the combine into the
+ *     expert epilogue (a variant; the pages apply them where combine takes
+ *     them): y[p] = bf16(recv_w[p] * (h Wd_e^T)[p]), the weight of the row's
+ *     (token, k) pair, written by moe_dispatch, multiplying the fp32
+ *     accumulators before the one rounding.  Pair with moe_combine_ex and
+ *     SYM_COMBINE_UNWEIGHTED.
+ * Any other flag bit: SYM_EINVAL.
+ */
+#define SYM_FFN_WEIGHTED_ROWS 1
+int moe_expert_ffn_ex(const sym_heap *h, const uint16_t *w_gate, const uint16_t *w_up,
+                      const uint16_t *w_down, int flags, symmoe_stream_t stream);
+
+/*
  * moe_combine: the weighted all-to-all gather of "Zero-copy MoE dispatch":
  *   out[g] = bf16( sum_{j<k} w[g][j] * y[slot(idx[g][j])][pos[g][j]] ),
  * fp32 accumulation in j order.
@@ -200,20 +214,38 @@ int moe_expert_ffn(const sym_heap *h, const uint16_t *w_gate, const uint16_t *w_
 int moe_combine(const sym_heap *h, const uint16_t *expert_out, const int32_t *idx,
                 const float *w, uint16_t *out, symmoe_stream_t stream);
 
+/*
+ * moe_combine_ex: moe_combine with flags (0: identical to it).
+ *   SYM_COMBINE_UNWEIGHTED: the rows already carry their weights
+ *     (SYM_FFN_WEIGHTED_ROWS): out[g] = bf16(sum_{j<k} y[slot(idx[g][j])][pos[g][j]]),
+ *     fp32 sum in j order; w is not read and may be NULL.
+ * Any other flag bit: SYM_EINVAL.
+ */
+#define SYM_COMBINE_UNWEIGHTED 1
+int moe_combine_ex(const sym_heap *h, const uint16_t *expert_out, const int32_t *idx,
+                   const float *w, uint16_t *out, int flags, symmoe_stream_t stream);
+
 /* Number of fallback copies moe_combine has made in this process. */
 uint64_t moe_combine_fallback_copies(void);
 
 /*
  * moe_pipeline: route -> dispatch -> expert FFN -> combine on one stream.
- *   fused = 0: one launch per stage (7 kernels).
- *   fused = 1: one persistent launch ("Mega-MoE"): expert tiles start as soon
- *              as the ready counters of their rows land.
+ *   mode bits:
+ *   SYM_PIPE_FUSED (1): one persistent launch ("Mega-MoE"): expert tiles start
+ *     as soon as the ready counters of their rows land; without it one launch
+ *     per stage (7 kernels).
+ *   SYM_PIPE_WEIGHTS_IN_FFN (2): routing weights applied in the expert
+ *     epilogue and an unweighted combine (SYM_FFN_WEIGHTED_ROWS,
+ *     SYM_COMBINE_UNWEIGHTED).
+ *   Any other bit: SYM_EINVAL.  mode 0 / 1 are the staged / fused pipeline.
  *   idx, w: device [N][k] outputs of the routing step; out: device [N][H].
  *   Bumps h->epoch.
  */
+#define SYM_PIPE_FUSED 1
+#define SYM_PIPE_WEIGHTS_IN_FFN 2
 int moe_pipeline(sym_heap *h, const float *logits, const uint16_t *x, const uint16_t *w_gate,
                  const uint16_t *w_up, const uint16_t *w_down, int32_t *idx, float *w,
-                 uint16_t *out, int fused, symmoe_stream_t stream);
+                 uint16_t *out, int mode, symmoe_stream_t stream);
 
 /*
  * sym_heap_status: synchronises `stream`, reads the heap status word (slot 0)

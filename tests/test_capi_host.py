@@ -129,7 +129,10 @@ def test_calls_reject_bad_pointers_without_device_work():
         lambda: sm.moe_dispatch(d, A + 8, A, A, 0),          # x not 16-byte aligned
         lambda: sm.moe_expert_ffn(d, A, None, A, 0),
         lambda: sm.moe_combine(d, None, A, A, A + 2, 0),     # out misaligned
-        lambda: sm.moe_pipeline(d, A, A, A, A, A, A, A, A, 2, 0),  # fused must be 0/1
+        lambda: sm.moe_pipeline(d, A, A, A, A, A, A, A, A, 4, 0),  # unknown mode bit
+        lambda: sm.moe_expert_ffn_ex(d, A, A, A, 2, 0),      # unknown flag
+        lambda: sm.moe_combine_ex(d, None, A, A, A, 2, 0),   # unknown flag
+        lambda: sm.moe_combine_ex(d, None, A, None, A, 0, 0),  # weighted combine needs w
     ]
     for c in cases:
         with pytest.raises(sm.SymmoeError) as ei:

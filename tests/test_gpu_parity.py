@@ -381,3 +381,60 @@ def test_ready_counter_timeout_returns_with_status(sm):
     _, _, _, out = run_gpu_stages(sm, cfg, logits, x, wg, wu, wd, heap=heap, idx=idx, w=w)
     assert heap.status() == 0
     assert torch.equal(out.view(torch.int16), out_ok.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "allk", "multi"])
+def test_weights_in_ffn_variant(sm, name):
+    """Routing weights applied in the down epilogue (recv_w) and an unweighted
+    combine, staged and fused, against the oracle variant; staged and fused
+    agree bit for bit."""
+    cfg = SMALL[name]
+    logits, x, wg, wu, wd = device_inputs(cfg, DEV)
+    n, k, H = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"], cfg["hidden"]
+    ref = oracle.pipeline(ms.logits_np(cfg), ms.x_np(cfg), cfg, fresh_weight_fn(cfg, DEV), weights_in_ffn=True)
+    runs = []
+    for fused in (0, 1):
+        heap = sm.SymHeap(cfg, DEV)
+        idx = torch.empty((n, k), dtype=torch.int32, device=DEV)
+        w = torch.empty((n, k), dtype=torch.float32, device=DEV)
+        out = torch.full((n, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+        heap.pipeline(logits, x, wg, wu, wd, idx, w, out, fused=fused, weights_in_ffn=True)
+        torch.cuda.synchronize()
+        assert heap.status() == 0
+        for d in range(cfg["world"]):
+            t = int(ref["total_recv"][d])
+            assert_close(bits(heap.y(d)[:t]), bf16_f64(ref["y"][d]), f"{name} weighted y slot {d}")
+        assert_close(bits(out), bf16_f64(ref["out"]), f"{name} fused={fused} out")
+        runs.append((heap, out))
+    (hs, os_), (hf, of) = runs
+    assert torch.equal(os_.view(torch.int16), of.view(torch.int16))
+    for d in range(cfg["world"]):
+        t = int(ref["total_recv"][d])
+        assert torch.equal(hs.y(d)[:t].view(torch.int16), hf.y(d)[:t].view(torch.int16))
+
+
+def test_weights_in_ffn_staged_calls(sm):
+    """The _ex calls one by one equal the pipeline mode, and an unweighted
+    combine of unweighted rows is the plain sum of the expert rows."""
+    cfg = SMALL["ragged"]
+    logits, x, wg, wu, wd = device_inputs(cfg, DEV)
+    n, k, H = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"], cfg["hidden"]
+    heap = sm.SymHeap(cfg, DEV)
+    idx = torch.empty((n, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((n, k), dtype=torch.float32, device=DEV)
+    a = torch.empty((n, H), dtype=torch.bfloat16, device=DEV)
+    b = torch.empty_like(a)
+    heap.pipeline(logits, x, wg, wu, wd, idx, w, a, weights_in_ffn=True)
+    heap.route_topk(logits, idx, w)
+    heap.dispatch(x, idx, w)
+    heap.expert_ffn(wg, wu, wd, weighted_rows=True)
+    heap.combine(idx, None, b, unweighted=True)        # w not read
+    torch.cuda.synchronize()
+    assert heap.status() == 0
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    ref = oracle.pipeline(ms.logits_np(cfg), ms.x_np(cfg), cfg, fresh_weight_fn(cfg, DEV))
+    heap.expert_ffn(wg, wu, wd)                          # plain rows again
+    heap.combine(idx, None, b, unweighted=True)
+    torch.cuda.synchronize()
+    plain = oracle.combine_sum(ref["y"], ref["idx"], ref["pos"], cfg["num_experts"], cfg["world"])
+    assert_close(bits(b), bf16_f64(plain), "unweighted combine of plain rows")
