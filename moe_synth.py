@@ -42,6 +42,7 @@ STREAM_WG = 3
 STREAM_WU = 4
 STREAM_WD = 5
 STREAM_PERM = 6
+STREAM_WR = 7  # router (gate) weights [E, H]
 
 LOGIT_SIGMA = 1.0
 X_SIGMA = 1.0
@@ -193,6 +194,12 @@ def weight_np(cfg: dict, which: str, expert: int, seed: int = 0) -> np.ndarray:
                     expert * per, per).reshape(rows, cols)
 
 
+def router_weight_np(cfg: dict, seed: int = 0) -> np.ndarray:
+    """bf16 bit patterns of the router weight Wr [E, H] (logits = x Wr^T)."""
+    e, h = cfg["num_experts"], cfg["hidden"]
+    return _chunked(lambda ix: normal_bf16_np(seed, STREAM_WR, ix, W_SIGMA), 0, e * h).reshape(e, h)
+
+
 def bf16_bits_to_f32_np(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
@@ -280,6 +287,13 @@ def weight_expert_torch(cfg: dict, which: str, expert: int, device, seed: int = 
     rows, cols = (i, h) if which in ("gate", "up") else (h, i)
     out = torch.empty((rows, cols), dtype=torch.bfloat16, device=device)
     return fill_normal_bf16_torch(out, seed, stream, expert * rows * cols, W_SIGMA)
+
+
+def router_weight_torch(cfg: dict, device, seed: int = 0):
+    """Router weight Wr [E, H] bf16 on ``device`` (the bits of ``router_weight_np``)."""
+    import torch
+    out = torch.empty((cfg["num_experts"], cfg["hidden"]), dtype=torch.bfloat16, device=device)
+    return fill_normal_bf16_torch(out, seed, STREAM_WR, 0, W_SIGMA)
 
 
 def weights_torch(cfg: dict, device, seed: int = 0):

@@ -19,6 +19,7 @@ and invariants their absolute values are parity-unpinned.
 from .moe import (  # noqa: F401
     bf16_bits_to_f64,
     round_f64_to_bf16_bits,
+    router_logits,
     route_topk,
     count_experts,
     place_pairs,

@@ -64,6 +64,16 @@ def slot_address(win_base: int, peer: int, per_rank_size: int, offset: int) -> i
 
 
 # ---------------------------------------------------------------------------
+# next: the router (gate) GEMM that produces the logits
+# ---------------------------------------------------------------------------
+
+def router_logits(x_bits: np.ndarray, wr_bits: np.ndarray) -> np.ndarray:
+    """logits[g, e] = fp32( sum_h x[g, h] * Wr[e, h] ), the products and the
+    sum in fp64 (x: [N, H] bf16 bits, Wr: [E, H] bf16 bits)."""
+    return (bf16_bits_to_f64(x_bits) @ bf16_bits_to_f64(wr_bits).T).astype(np.float32)
+
+
+# ---------------------------------------------------------------------------
 # a1: routing (the pages take indices/weights as dispatch inputs)
 # ---------------------------------------------------------------------------
 

@@ -326,3 +326,38 @@ def test_weights_in_ffn_exact_on_integer_ffn():
     w = np.array([0.5, 0.25, 2.0, 1.0, 0.125, 4.0], dtype=np.float32)
     yw = oracle.scale_rows([ye], [w])[0]
     assert np.array_equal(oracle.bf16_bits_to_f64(yw), y_ref * w[:, None])
+
+
+# ------------------------------------------------------- router (gate) GEMM
+
+def test_router_logits_one_hot_rows_pick_columns():
+    rng = np.random.default_rng(5)
+    wr = _bits(rng.standard_normal((6, 32)))
+    x = np.zeros((4, 32), dtype=np.float32)
+    cols = [0, 7, 31, 12]
+    for r, c in enumerate(cols):
+        x[r, c] = 1.0
+    lg = oracle.router_logits(_bits(x), wr)
+    assert lg.dtype == np.float32 and lg.shape == (4, 6)
+    for r, c in enumerate(cols):
+        assert np.array_equal(lg[r], oracle.bf16_bits_to_f64(wr)[:, c].astype(np.float32))
+
+
+def test_router_logits_integer_exact_and_orientation():
+    # small integers: every product and sum is exact; E = H so a transposed
+    # operand would still have the right shape and must be caught by value
+    x = np.array([[1, 2, 0, -1], [3, 0, 1, 1]], dtype=np.float32)
+    wr = np.array([[1, 0, 0, 0], [0, 1, 0, 2], [1, 1, 1, 1], [-2, 0, 3, 0]], dtype=np.float32)
+    lg = oracle.router_logits(_bits(x), _bits(wr))
+    assert lg.tolist() == [[1, 0, 2, -2], [3, 1, 5, -3]]
+    assert not np.array_equal(lg, (x @ wr).astype(np.float32))
+
+
+def test_router_logits_matches_torch_cpu_fp32():
+    cfg = ms.CONFIGS["tiny"]
+    x = ms.x_np(cfg)
+    wr = ms.router_weight_np(cfg)
+    lg = oracle.router_logits(x, wr)
+    t = lambda b: torch.from_numpy(oracle.bf16_bits_to_f64(b).astype(np.float32))
+    ref = (t(x) @ t(wr).T).numpy()
+    assert np.allclose(lg, ref, rtol=1e-5, atol=1e-6)
