@@ -36,6 +36,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--config", default="mixtral")
     p.add_argument("--fused", action="store_true", help="single-launch pipeline")
+    p.add_argument("--with-router", action="store_true",
+                   help="start each step from the token activations: the router GEMM produces the logits")
     p.add_argument("--weights-in-ffn", action="store_true",
                    help="routing weights applied in the expert epilogue, unweighted combine")
     p.add_argument("--unfused", action="store_true",
@@ -81,14 +83,15 @@ def l2_statement(cfg: dict) -> str:
             "a small-case timing, not a roofline measurement")
 
 
-def workload_config(name: str, cfg: dict, fused: bool, weights_in_ffn: bool = False) -> dict:
+def workload_config(name: str, cfg: dict, fused: bool, weights_in_ffn: bool = False,
+                    with_router: bool = False) -> dict:
     import moe_synth as ms
     n = cfg["world"] * cfg["tokens_per_slot"]
     return {"workload": ms.CONFIG_TITLES.get(name, name), "preset": name,
             "world_slots": cfg["world"], "tokens_per_slot": cfg["tokens_per_slot"],
             "tokens_per_step": n, "hidden": cfg["hidden"], "inter": cfg["inter"],
             "experts": cfg["num_experts"], "topk": cfg["topk"], "fused": bool(fused),
-            "weights_in_ffn": bool(weights_in_ffn),
+            "weights_in_ffn": bool(weights_in_ffn), "with_router": bool(with_router),
             "l2": l2_statement(cfg),
             "parallelism": "replicas"}
 
@@ -312,12 +315,14 @@ def run_ours(args):
     cfg = get_cfg(args)
     fused = 1 if (args.fused or (cfg.get("fused") and not args.unfused)) else 0
     wif = bool(getattr(args, "weights_in_ffn", False))
+    with_router = bool(getattr(args, "with_router", False))
     n, k, H = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"], cfg["hidden"]
 
     heap = sm.SymHeap(cfg, dev)
     logits = ms.logits_torch(cfg, dev)
     x = ms.x_torch(cfg, dev)
     wg, wu, wd = ms.weights_torch(cfg, dev)
+    wr = ms.router_weight_torch(cfg, dev) if with_router else None
     idx = torch.empty((n, k), dtype=torch.int32, device=dev)
     w = torch.empty((n, k), dtype=torch.float32, device=dev)
     out = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
@@ -331,16 +336,20 @@ def run_ours(args):
     # Stage-by-stage steps make the same four C-ABI calls that moe_pipeline
     # makes, with an event on the stream between stages, so every stage time
     # (and the expert FFN's roofline) is measured inside the timed region.
-    stage_names = ["route", "dispatch", "expert_ffn", "combine"]
-    stage_evs = [] if fused else [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    stage_names = (["router"] if with_router else []) + ["route", "dispatch", "expert_ffn", "combine"]
+    nst = len(stage_names)
+    stage_evs = [] if fused else [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
                                   for _ in range(args.steps)]
 
     def step(i=None):
         if fused:
+            if with_router:
+                heap.router_logits(x, wr, logits, stream=stream)
             heap.pipeline(logits, x, wg, wu, wd, idx, w, out, fused=1, weights_in_ffn=wif, stream=stream)
             return
         ev = stage_evs[i] if i is not None else None
-        calls = [lambda: heap.route_topk(logits, idx, w, stream=stream),
+        calls = ([lambda: heap.router_logits(x, wr, logits, stream=stream)] if with_router else []) + [
+                 lambda: heap.route_topk(logits, idx, w, stream=stream),
                  lambda: heap.dispatch(x, idx, w, stream=stream),
                  lambda: heap.expert_ffn(wg, wu, wd, weighted_rows=wif, stream=stream),
                  lambda: heap.combine(idx, w, out, unweighted=wif, stream=stream)]
@@ -349,7 +358,7 @@ def run_ours(args):
                 ev[j].record(stream)
             call()
         if ev:
-            ev[4].record(stream)
+            ev[nst].record(stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -376,9 +385,9 @@ def run_ours(args):
     # ---- stage times: averages over the timed steps (device time per stage)
     stages = {}
     if not fused:
-        acc = [0.0] * 4
+        acc = [0.0] * nst
         for ev in stage_evs:
-            for j in range(4):
+            for j in range(nst):
                 acc[j] += ev[j].elapsed_time(ev[j + 1])
         stages = dict(zip(stage_names, [a / args.steps for a in acc]))
 
@@ -423,6 +432,14 @@ def run_ours(args):
         }
         stage_bw["dispatch_frac"] = stage_bw["dispatch_gbs"] / hbm
         stage_bw["combine_frac"] = stage_bw["combine_gbs"] / hbm
+        if "router" in stages:
+            # router GEMM: reads x [N,H] and Wr [E,H] (bf16), writes logits [N,E] (fp32)
+            rbytes = n * H * 2 + cfg["num_experts"] * H * 2 + n * cfg["num_experts"] * 4
+            rflops = 2.0 * n * H * cfg["num_experts"]
+            rs = stages["router"] / 1e3
+            stage_bw["router_gbs"] = rbytes / rs / 1e9
+            stage_bw["router_tflops"] = rflops / rs / 1e12
+            stage_bw["router_frac"] = max(stage_bw["router_gbs"] / hbm, stage_bw["router_tflops"] / tf_peak)
 
     # ---- end to end through the public API with host buffers
     # Every step copies its inputs (logits, x) from pinned host memory and reads
@@ -452,13 +469,16 @@ def run_ours(args):
                 with torch.cuda.stream(s_up):
                     if computed[b] is not None:
                         s_up.wait_event(computed[b])
-                    lg_d[b].copy_(lg_h, non_blocking=True)
+                    if not with_router:  # with the router the step starts from x alone
+                        lg_d[b].copy_(lg_h, non_blocking=True)
                     x_d[b].copy_(x_h, non_blocking=True)
                     up = ev()
                     up.record(s_up)
                 stream.wait_event(up)
                 if downloaded[b] is not None:
                     stream.wait_event(downloaded[b])
+                if with_router:
+                    heap.router_logits(x_d[b], wr, lg_d[b], stream=stream)
                 heap.pipeline(lg_d[b], x_d[b], wg, wu, wd, idx, w, out_d[b], fused=fused, weights_in_ffn=wif,
                               stream=stream)
                 computed[b] = ev()
@@ -482,7 +502,7 @@ def run_ours(args):
         assert torch.equal(out_h[(e_steps - 1) & 1].view(torch.int16), out.cpu().view(torch.int16)), \
             "end-to-end output differs from the device-resident run"
         e2e = {"value": n * e_steps * world / (e_ms / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": lg_h.numel() * 4 + x_h.numel() * 2,
+               "h2d_bytes_per_step": (0 if with_router else lg_h.numel() * 4) + x_h.numel() * 2,
                "d2h_bytes_per_step": out_h[0].numel() * 2, "steps": e_steps,
                "overlap": "uploads and downloads on their own streams, double-buffered"}
 
@@ -503,7 +523,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(args.config, cfg, fused, wif),
+            "config": workload_config(args.config, cfg, fused, wif, with_router),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),

@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
         L.sym_heap_slot_ptr.argtypes = [P(SymHeapDesc), ctypes.c_int, _u64]
         L.sym_heap_slot_ptr.restype = _vp
         L.moe_route_topk.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
+        L.moe_router_logits.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
         L.moe_dispatch.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
         L.moe_expert_ffn.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
         L.moe_expert_ffn_ex.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, ctypes.c_int, _vp]
@@ -154,6 +155,11 @@ def sym_heap_slot_ptr(heap: SymHeapDesc, slot: int, offset: int) -> int | None:
 def moe_route_topk(heap: SymHeapDesc, logits, idx, w, stream=None) -> None:
     _check(lib().moe_route_topk(ctypes.byref(heap), _ptr(logits), _ptr(idx), _ptr(w),
                                 _stream(stream)), "moe_route_topk")
+
+
+def moe_router_logits(heap: SymHeapDesc, x, w_router, logits, stream=None) -> None:
+    _check(lib().moe_router_logits(ctypes.byref(heap), _ptr(x), _ptr(w_router), _ptr(logits),
+                                   _stream(stream)), "moe_router_logits")
 
 
 def moe_dispatch(heap: SymHeapDesc, x, idx, w, stream=None) -> None:
@@ -293,6 +299,9 @@ class SymHeap:
     # calls -----------------------------------------------------------------
     def route_topk(self, logits, idx, w, stream=None):
         moe_route_topk(self.desc, logits, idx, w, stream)
+
+    def router_logits(self, x, w_router, logits, stream=None):
+        moe_router_logits(self.desc, x, w_router, logits, stream)
 
     def dispatch(self, x, idx, w, stream=None):
         moe_dispatch(self.desc, x, idx, w, stream)

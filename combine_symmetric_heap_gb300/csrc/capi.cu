@@ -22,6 +22,8 @@ cudaError_t launch_expert_ffn(const sym_heap &h, const uint16_t *wg, const uint1
                               cudaStream_t st);
 cudaError_t launch_combine(const sym_heap &h, const uint16_t *expert_out, const int32_t *idx,
                            const float *w, uint16_t *out, int unit_weights, int num_sms, cudaStream_t st);
+cudaError_t launch_router(const sym_heap &h, const uint16_t *x, const uint16_t *wr, float *logits,
+                          int num_sms, cudaStream_t st);
 size_t fused_ctrl_bytes(const moe_shape &s);
 cudaError_t launch_fused(const sym_heap &h, const float *logits, const uint16_t *x,
                          const uint16_t *wg, const uint16_t *wu, const uint16_t *wd,
@@ -176,6 +178,14 @@ int moe_route_topk(const sym_heap *h, const float *logits, int32_t *idx, float *
                    symmoe_stream_t stream) {
   if (!heap_ok(h) || !aligned4(logits) || !aligned4(idx) || !aligned4(w)) return SYM_EINVAL;
   return from_cuda(launch_route_topk(*h, logits, idx, w, (cudaStream_t)stream));
+}
+
+int moe_router_logits(const sym_heap *h, const uint16_t *x, const uint16_t *w_router, float *logits,
+                      symmoe_stream_t stream) {
+  if (!heap_ok(h) || !aligned16(x) || !aligned16(w_router) || !aligned4(logits)) return SYM_EINVAL;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return SYM_ECUDA;
+  return from_cuda(launch_router(*h, x, w_router, logits, sms, (cudaStream_t)stream));
 }
 
 int moe_dispatch(sym_heap *h, const uint16_t *x, const int32_t *idx, const float *w,

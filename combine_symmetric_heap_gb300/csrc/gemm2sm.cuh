@@ -65,16 +65,18 @@ __host__ __device__ inline int box_index(int half_rows) {
   while (i < NBOX - 1 && (BOX_MIN_ROWS << i) < half_rows) ++i;
   return i;
 }
-enum Kind : int { GATE_UP = 0, DOWN = 1 };
+// GATE_UP: h = silu(x Wg^T) * x Wu^T;  DOWN: y = h Wd^T;  ROUTER: logits = x Wr^T
+// (one pseudo-expert over the N tokens, fp32 output)
+enum Kind : int { GATE_UP = 0, DOWN = 1, ROUTER = 2 };
 
 // features per pair tile and K blocks per kind
 __host__ __device__ inline int feat_of(int kind) { return kind == GATE_UP ? 128 : 256; }
 __host__ __device__ inline int nf_of(const sym_heap &h, int kind) {
-  const int n = kind == GATE_UP ? h.s.inter : h.s.hidden;
+  const int n = kind == GATE_UP ? h.s.inter : kind == DOWN ? h.s.hidden : h.s.num_experts;
   return (n + feat_of(kind) - 1) / feat_of(kind);
 }
 __host__ __device__ inline int nk_of(const sym_heap &h, int kind) {
-  return (kind == GATE_UP ? h.s.hidden : h.s.inter) / BK;
+  return (kind == DOWN ? h.s.inter : h.s.hidden) / BK;
 }
 
 struct TileInfo {
@@ -324,6 +326,7 @@ struct Pipe {
   const volatile int *stop;   // roles stop before tile index *stop
   uint32_t tmo;               // wait limit, microseconds
   int scale_rows;             // DOWN: y row p = bf16(recv_w[p] * acc) (weights in the epilogue)
+  float *logits;              // ROUTER: the [N][E] fp32 output
 };
 
 __device__ __forceinline__ void ring_advance(int &stage, uint32_t &phase) {
@@ -501,6 +504,20 @@ __device__ void epi_rows(const sym_heap &h, const Pipe &p, const TileInfo &ti, u
         const float up = is_gate ? other : mine;
         if (col < nrows) out[(size_t)col * ld] = to_bf16(__fdividef(gt, 1.0f + __expf(-gt)) * up);
       }
+    }
+  } else if (KIND == ROUTER) {
+    const int ld = h.s.num_experts;
+    const int feature = ti.f * 256 + (int)p.rank * 128 + q * 32 + lane;  // expert of this lane
+    float *out = p.logits + (size_t)row * ld + feature;
+    const bool live = feature < ld;
+    for (int c0 = 0; c0 < nrows; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tcol + c0, v);
+      tmem_ld_wait();
+      if (c0 == 0) head();
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (live && c0 + c < nrows) out[(size_t)(c0 + c) * ld] = __uint_as_float(v[c]);
     }
   } else {
     const int ld = h.s.hidden;

@@ -160,6 +160,20 @@ int moe_route_topk(const sym_heap *h, const float *logits, int32_t *idx, float *
                    symmoe_stream_t stream);
 
 /*
+ * moe_router_logits: the router (gate) GEMM that produces the routing logits
+ * from the token activations (the step before moe_route_topk; the pages take
+ * the routing as given):
+ *   logits[g][e] = sum_h x[g][h] * w_router[e][h],  fp32 accumulation on the
+ *   tensor cores, fp32 output.
+ *   x: device [N][H] bf16 (16-byte aligned);  w_router: device [E][H] bf16
+ *   (16-byte aligned);  logits: device [N][E] fp32.  N, H, E from the heap's
+ *   shape; the heap is read for its shape and status word only.
+ * Returns SYM_OK, SYM_EINVAL (pointer/alignment) or SYM_ECUDA; asynchronous.
+ */
+int moe_router_logits(const sym_heap *h, const uint16_t *x, const uint16_t *w_router, float *logits,
+                      symmoe_stream_t stream);
+
+/*
  * moe_dispatch: the all-to-all scatter of "Zero-copy MoE dispatch".
  * Counts pairs per expert, builds receive offsets, and copies every token row
  * x[g] into slot (idx[g][j] / (E/W))'s recv_x window at its receive row

@@ -1,0 +1,75 @@
+"""The router (gate) GEMM on the GPU against the oracle: fp32 logits within a
+tolerance derived from fp32 accumulation (bf16 products are exact in fp32; an
+H-term fp32 sum is off by at most about sqrt(H) ulps of its partial sums), and
+the routing taken from those logits, which must be bit-exact on both sides
+because both route the same fp32 values."""
+import numpy as np
+import pytest
+import torch
+
+import moe_synth as ms
+import oracle
+from _cases import SMALL
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def sm():
+    import combine_symmetric_heap_gb300 as m
+    return m
+
+
+def _check_logits(got, ref, what):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    diff = np.abs(got - ref)
+    assert np.all(diff <= 1e-3 * np.maximum(1.0, np.abs(ref))), f"{what}: max diff {diff.max()}"
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert rel <= 1e-4, f"{what}: relative L2 {rel}"
+
+
+def _run(sm, cfg):
+    n = cfg["world"] * cfg["tokens_per_slot"]
+    heap = sm.SymHeap(cfg, DEV)
+    x = ms.x_torch(cfg, DEV)
+    wr = ms.router_weight_torch(cfg, DEV)
+    logits = torch.full((n, cfg["num_experts"]), float("nan"), dtype=torch.float32, device=DEV)
+    heap.router_logits(x, wr, logits)
+    torch.cuda.synchronize()
+    assert heap.status() == 0
+    return heap, logits
+
+
+CASES = dict(SMALL)
+CASES["wide_e"] = dict(world=3, tokens_per_slot=90, hidden=256, num_experts=300, topk=4, inter=128)
+CASES["remainder"] = dict(world=2, tokens_per_slot=135, hidden=384, num_experts=8, topk=2, inter=128)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_router_small(sm, name):
+    cfg = CASES[name]
+    heap, logits = _run(sm, cfg)
+    ref = oracle.router_logits(ms.x_np(cfg), ms.router_weight_np(cfg))
+    got = logits.cpu().numpy()
+    _check_logits(got, ref, name)
+    # routing of the GPU logits: both sides decide on the same fp32 values
+    k = cfg["topk"]
+    n = got.shape[0]
+    idx = torch.empty((n, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((n, k), dtype=torch.float32, device=DEV)
+    heap.route_topk(logits, idx, w)
+    ri, rw = oracle.route_topk(got, k)
+    assert np.array_equal(idx.cpu().numpy(), ri)
+
+
+@pytest.mark.parametrize("name,rows", [("mixtral", 256), ("deepseek", 128)])
+def test_router_full_size_sampled(sm, name, rows):
+    cfg = ms.CONFIGS[name]
+    heap, logits = _run(sm, cfg)
+    n = cfg["world"] * cfg["tokens_per_slot"]
+    pick = np.sort(np.random.default_rng(2).choice(n, size=rows, replace=False))
+    ref = oracle.router_logits(ms.x_np(cfg, rows=pick), ms.router_weight_np(cfg))
+    _check_logits(logits[torch.from_numpy(pick).to(DEV)].cpu().numpy(), ref, name)
+    assert torch.isfinite(logits).all()
