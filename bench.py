@@ -380,7 +380,7 @@ def run_ours(args):
     assert heap.status(stream=stream) == 0, "device status word set during the timed steps"
     ms_step = ms_total / args.steps
     value = n * args.steps * world / (ms_total / 1e3)
-    launches_per_step = 1 if fused else 7
+    launches_per_step = (1 if fused else 7) + (1 if with_router else 0)
 
     # ---- stage times: averages over the timed steps (device time per stage)
     stages = {}
