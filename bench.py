@@ -336,23 +336,23 @@ def run_ours(args):
     # Stage-by-stage steps make the same four C-ABI calls that moe_pipeline
     # makes, with an event on the stream between stages, so every stage time
     # (and the expert FFN's roofline) is measured inside the timed region.
-    stage_names = (["router"] if with_router else []) + ["route", "dispatch", "expert_ffn", "combine"]
+    # The fused step is one launch (plus the router's, when it is timed too).
+    stage_names = (["router"] if with_router else []) + (
+        ["fused"] if fused else ["route", "dispatch", "expert_ffn", "combine"])
     nst = len(stage_names)
-    stage_evs = [] if fused else [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
-                                  for _ in range(args.steps)]
+    stage_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
 
     def step(i=None):
-        if fused:
-            if with_router:
-                heap.router_logits(x, wr, logits, stream=stream)
-            heap.pipeline(logits, x, wg, wu, wd, idx, w, out, fused=1, weights_in_ffn=wif, stream=stream)
-            return
         ev = stage_evs[i] if i is not None else None
-        calls = ([lambda: heap.router_logits(x, wr, logits, stream=stream)] if with_router else []) + [
-                 lambda: heap.route_topk(logits, idx, w, stream=stream),
-                 lambda: heap.dispatch(x, idx, w, stream=stream),
-                 lambda: heap.expert_ffn(wg, wu, wd, weighted_rows=wif, stream=stream),
-                 lambda: heap.combine(idx, w, out, unweighted=wif, stream=stream)]
+        calls = [lambda: heap.router_logits(x, wr, logits, stream=stream)] if with_router else []
+        if fused:
+            calls.append(lambda: heap.pipeline(logits, x, wg, wu, wd, idx, w, out, fused=1,
+                                               weights_in_ffn=wif, stream=stream))
+        else:
+            calls += [lambda: heap.route_topk(logits, idx, w, stream=stream),
+                      lambda: heap.dispatch(x, idx, w, stream=stream),
+                      lambda: heap.expert_ffn(wg, wu, wd, weighted_rows=wif, stream=stream),
+                      lambda: heap.combine(idx, w, out, unweighted=wif, stream=stream)]
         for j, call in enumerate(calls):
             if ev:
                 ev[j].record(stream)
@@ -380,16 +380,16 @@ def run_ours(args):
     assert heap.status(stream=stream) == 0, "device status word set during the timed steps"
     ms_step = ms_total / args.steps
     value = n * args.steps * world / (ms_total / 1e3)
-    launches_per_step = (1 if fused else 7) + (1 if with_router else 0)
+    # the router is one GEMM launch, plus one reduction launch when it splits K
+    router_launches = (1 + (heap.router_splits() > 1)) if with_router else 0
+    launches_per_step = (1 if fused else 7) + router_launches
 
     # ---- stage times: averages over the timed steps (device time per stage)
-    stages = {}
-    if not fused:
-        acc = [0.0] * nst
-        for ev in stage_evs:
-            for j in range(nst):
-                acc[j] += ev[j].elapsed_time(ev[j + 1])
-        stages = dict(zip(stage_names, [a / args.steps for a in acc]))
+    acc = [0.0] * nst
+    for ev in stage_evs:
+        for j in range(nst):
+            acc[j] += ev[j].elapsed_time(ev[j + 1])
+    stages = dict(zip(stage_names, [a / args.steps for a in acc]))
 
     experts_hit = int(sum(int((heap.cnt(d) > 0).sum().item()) for d in range(cfg["world"])))
     alg = algorithmic(cfg, experts_hit)
@@ -401,7 +401,7 @@ def run_ours(args):
     t_hbm = alg["ffn_bytes"] / (hbm * 1e9)
     bound = "tensor" if t_tensor >= t_hbm else "hbm"
     if fused:
-        kern_s = ms_step / 1e3  # one launch does the whole step
+        kern_s = stages["fused"] / 1e3  # one launch does the whole step
         kname = "moe_fused_kernel (whole step in one launch)"
         extra_bytes = alg["route_bytes"] + alg["dispatch_bytes"] + alg["combine_bytes"]
     else:
@@ -422,24 +422,22 @@ def run_ours(args):
                 "algorithmic_per_step": {"flops": alg["ffn_flops"], "bytes": alg["ffn_bytes"] + extra_bytes,
                                          "experts_hit": experts_hit},
                 "other_roof": other}
-    stage_bw = None
-    if stages:
-        stage_bw = {
-            "dispatch_gbs": alg["dispatch_bytes"] / (stages["dispatch"] / 1e3) / 1e9,
-            "combine_gbs": alg["combine_bytes"] / (stages["combine"] / 1e3) / 1e9,
-            "route_gbs": alg["route_bytes"] / (stages["route"] / 1e3) / 1e9,
-            "hbm_peak_gbs": hbm,
-        }
+    stage_bw = {"hbm_peak_gbs": hbm}
+    if not fused:
+        stage_bw["dispatch_gbs"] = alg["dispatch_bytes"] / (stages["dispatch"] / 1e3) / 1e9
+        stage_bw["combine_gbs"] = alg["combine_bytes"] / (stages["combine"] / 1e3) / 1e9
+        stage_bw["route_gbs"] = alg["route_bytes"] / (stages["route"] / 1e3) / 1e9
         stage_bw["dispatch_frac"] = stage_bw["dispatch_gbs"] / hbm
         stage_bw["combine_frac"] = stage_bw["combine_gbs"] / hbm
-        if "router" in stages:
-            # router GEMM: reads x [N,H] and Wr [E,H] (bf16), writes logits [N,E] (fp32)
-            rbytes = n * H * 2 + cfg["num_experts"] * H * 2 + n * cfg["num_experts"] * 4
-            rflops = 2.0 * n * H * cfg["num_experts"]
-            rs = stages["router"] / 1e3
-            stage_bw["router_gbs"] = rbytes / rs / 1e9
-            stage_bw["router_tflops"] = rflops / rs / 1e12
-            stage_bw["router_frac"] = max(stage_bw["router_gbs"] / hbm, stage_bw["router_tflops"] / tf_peak)
+    if "router" in stages:
+        # router GEMM: reads x [N,H] and Wr [E,H] (bf16), writes logits [N,E] (fp32)
+        rbytes = n * H * 2 + cfg["num_experts"] * H * 2 + n * cfg["num_experts"] * 4
+        rflops = 2.0 * n * H * cfg["num_experts"]
+        rs = stages["router"] / 1e3
+        stage_bw["router_gbs"] = rbytes / rs / 1e9
+        stage_bw["router_tflops"] = rflops / rs / 1e12
+        stage_bw["router_frac"] = max(stage_bw["router_gbs"] / hbm, stage_bw["router_tflops"] / tf_peak)
+        stage_bw["router_splits"] = heap.router_splits()
 
     # ---- end to end through the public API with host buffers
     # Every step copies its inputs (logits, x) from pinned host memory and reads

@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
         L.sym_heap_slot_ptr.restype = _vp
         L.moe_route_topk.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
         L.moe_router_logits.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
+        L.moe_router_splits.argtypes = [P(SymHeapDesc), P(ctypes.c_int)]
         L.moe_dispatch.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
         L.moe_expert_ffn.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
         L.moe_expert_ffn_ex.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, ctypes.c_int, _vp]
@@ -160,6 +161,12 @@ def moe_route_topk(heap: SymHeapDesc, logits, idx, w, stream=None) -> None:
 def moe_router_logits(heap: SymHeapDesc, x, w_router, logits, stream=None) -> None:
     _check(lib().moe_router_logits(ctypes.byref(heap), _ptr(x), _ptr(w_router), _ptr(logits),
                                    _stream(stream)), "moe_router_logits")
+
+
+def moe_router_splits(heap: SymHeapDesc) -> int:
+    out = ctypes.c_int(0)
+    _check(lib().moe_router_splits(ctypes.byref(heap), ctypes.byref(out)), "moe_router_splits")
+    return out.value
 
 
 def moe_dispatch(heap: SymHeapDesc, x, idx, w, stream=None) -> None:
@@ -302,6 +309,9 @@ class SymHeap:
 
     def router_logits(self, x, w_router, logits, stream=None):
         moe_router_logits(self.desc, x, w_router, logits, stream)
+
+    def router_splits(self) -> int:
+        return moe_router_splits(self.desc)
 
     def dispatch(self, x, idx, w, stream=None):
         moe_dispatch(self.desc, x, idx, w, stream)

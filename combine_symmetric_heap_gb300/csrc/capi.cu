@@ -24,6 +24,7 @@ cudaError_t launch_combine(const sym_heap &h, const uint16_t *expert_out, const 
                            const float *w, uint16_t *out, int unit_weights, int num_sms, cudaStream_t st);
 cudaError_t launch_router(const sym_heap &h, const uint16_t *x, const uint16_t *wr, float *logits,
                           int num_sms, cudaStream_t st);
+cudaError_t router_plan(const sym_heap &h, int num_sms, int *grid, int *splits, int *kb_per_split);
 size_t fused_ctrl_bytes(const moe_shape &s);
 cudaError_t launch_fused(const sym_heap &h, const float *logits, const uint16_t *x,
                          const uint16_t *wg, const uint16_t *wu, const uint16_t *wd,
@@ -186,6 +187,14 @@ int moe_router_logits(const sym_heap *h, const uint16_t *x, const uint16_t *w_ro
   const int sms = num_sms_of_current_device();
   if (sms <= 0) return SYM_ECUDA;
   return from_cuda(launch_router(*h, x, w_router, logits, sms, (cudaStream_t)stream));
+}
+
+int moe_router_splits(const sym_heap *h, int *splits) {
+  if (!heap_ok(h) || !splits) return SYM_EINVAL;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return SYM_ECUDA;
+  int grid, kb;
+  return from_cuda(router_plan(*h, sms, &grid, splits, &kb));
 }
 
 int moe_dispatch(sym_heap *h, const uint16_t *x, const int32_t *idx, const float *w,

@@ -66,13 +66,16 @@ __host__ __device__ inline int box_index(int half_rows) {
   return i;
 }
 // GATE_UP: h = silu(x Wg^T) * x Wu^T;  DOWN: y = h Wd^T;  ROUTER: logits = x Wr^T
-// (one pseudo-expert over the N tokens, fp32 output)
+// with the roles turned: tokens on the MMA's M side (the "features", 256 per
+// pair tile) and the E router rows on the N side (the "rows" of one
+// pseudo-expert), so a small E costs a narrow MMA instead of a padded one;
+// fp32 output.
 enum Kind : int { GATE_UP = 0, DOWN = 1, ROUTER = 2 };
 
 // features per pair tile and K blocks per kind
 __host__ __device__ inline int feat_of(int kind) { return kind == GATE_UP ? 128 : 256; }
 __host__ __device__ inline int nf_of(const sym_heap &h, int kind) {
-  const int n = kind == GATE_UP ? h.s.inter : kind == DOWN ? h.s.hidden : h.s.num_experts;
+  const int n = kind == GATE_UP ? h.s.inter : kind == DOWN ? h.s.hidden : h.s.world * h.s.tokens_per_slot;
   return (n + feat_of(kind) - 1) / feat_of(kind);
 }
 __host__ __device__ inline int nk_of(const sym_heap &h, int kind) {
@@ -81,6 +84,7 @@ __host__ __device__ inline int nk_of(const sym_heap &h, int kind) {
 
 struct TileInfo {
   int e, f, n, d, row0, valid;  // valid: token rows of the tile, up to BN + REM_MAX
+  int ks = 0;                   // K split of the tile (Pipe::kb_per_split K blocks each)
 };
 
 // Token tiles of an expert with c rows: BN rows each.  An expert with one
@@ -326,8 +330,15 @@ struct Pipe {
   const volatile int *stop;   // roles stop before tile index *stop
   uint32_t tmo;               // wait limit, microseconds
   int scale_rows;             // DOWN: y row p = bf16(recv_w[p] * acc) (weights in the epilogue)
-  float *logits;              // ROUTER: the [N][E] fp32 output
+  float *logits;              // ROUTER: the [N][E] fp32 output (split ks: its partial at ks*N*E)
+  int kb_per_split = 0;       // K blocks per split of a tile (0: the whole K)
 };
+
+// K blocks [kb0, kb1) of tile ti
+__device__ __forceinline__ void k_range(const Pipe &p, const TileInfo &ti, int nk, int &kb0, int &kb1) {
+  kb0 = p.kb_per_split ? ti.ks * p.kb_per_split : 0;
+  kb1 = p.kb_per_split ? min(nk, kb0 + p.kb_per_split) : nk;
+}
 
 __device__ __forceinline__ void ring_advance(int &stage, uint32_t &phase) {
   if (++stage == STAGES) {
@@ -347,11 +358,10 @@ template <int KIND, bool TWO, typename Probe>
 __device__ __forceinline__ bool produce_k(const sym_heap &h, const Pipe &p, ProdState &s, int d, int arow,
                                           int r0, int r1, const CUtensorMap *ma0, const CUtensorMap *ma1,
                                           const CUtensorMap *mb0, const CUtensorMap *mb1, uint32_t tx, int t,
-                                          Probe &probe) {
+                                          int kb0, int kb1, Probe &probe) {
   const uint32_t full_leader = map_to(&p.full[0], 0);
-  const int nk = nk_of(h, KIND);
-  for (int kb = 0; kb < nk; ++kb) {
-    if (kb == nk / 2) probe();
+  for (int kb = kb0; kb < kb1; ++kb) {
+    if (kb == (kb0 + kb1) / 2) probe();
     if (!wait_or_stop(&p.empty[s.stage], s.phase ^ 1u, t, p.stop, p.abort, p.tmo, h)) return false;
     uint8_t *sb = p.ring + (size_t)s.stage * STAGE_BYTES;
     const uint32_t bar = full_leader + (uint32_t)(s.stage * sizeof(uint64_t));
@@ -385,10 +395,12 @@ __device__ bool produce_tile(const sym_heap &h, const Pipe &p, ProdState &s, con
   const int r1 = ti.row0 + BN + (int)p.rank * half1;
   const int arow = KIND == GATE_UP ? ti.e * h.s.inter + ti.f * 128 + (int)p.rank * 64
                                    : ti.e * h.s.hidden + ti.f * 256 + (int)p.rank * 128;
+  int kb0, kb1;
+  k_range(p, ti, nk_of(h, KIND), kb0, kb1);
   return g.n1 ? produce_k<KIND, true>(h, p, s, ti.d, arow, r0, r1, ma0, ma1, &mb.m[box0], &mb.m[box1], tx, t,
-                                      probe)
+                                      kb0, kb1, probe)
               : produce_k<KIND, false>(h, p, s, ti.d, arow, r0, r1, ma0, ma1, &mb.m[box0], &mb.m[box1], tx,
-                                       t, probe);
+                                       t, kb0, kb1, probe);
 }
 
 struct MmaState {
@@ -410,9 +422,8 @@ __device__ __forceinline__ bool acquire(const sym_heap &h, const Pipe &p, uint64
 // MMA K loop of one tile into d0 (and, TWO, the remainder into d1).
 template <int KIND, bool TWO>
 __device__ __forceinline__ bool mma_k(const sym_heap &h, const Pipe &p, MmaState &s, uint32_t d0, uint32_t d1,
-                                      uint32_t idesc0, uint32_t idesc1, int t) {
-  const int nk = nk_of(h, KIND);
-  for (int kb = 0; kb < nk; ++kb) {
+                                      uint32_t idesc0, uint32_t idesc1, int kb0, int kb1, int t) {
+  for (int kb = kb0; kb < kb1; ++kb) {
     if (!wait_or_stop(&p.full[s.stage], s.phase, t, p.stop, p.abort, p.tmo, h)) return false;
     tc_fence_after();
     uint8_t *sb = p.ring + (size_t)s.stage * STAGE_BYTES;
@@ -421,7 +432,7 @@ __device__ __forceinline__ bool mma_k(const sym_heap &h, const Pipe &p, MmaState
 #pragma unroll
     for (int kk = 0; kk < BK / UK; ++kk) {
       const uint64_t adv = (uint64_t)(kk * UK * 2 / 16);
-      const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+      const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
       mma2(d0, da + adv, db0 + adv, idesc0, acc);
       if (TWO) mma2(d1, da + adv, db1 + adv, idesc1, acc);  // interleaved: issues faster than grouped
     }
@@ -444,8 +455,10 @@ __device__ bool mma_tile(const sym_heap &h, const Pipe &p, MmaState &s, const Ti
   const uint32_t d0 = p.tmem_base + (uint32_t)(b * ACC_COLS);
   const uint32_t d1 = p.tmem_base + (uint32_t)((b ^ 1) * ACC_COLS);
   const uint32_t idesc0 = idesc_bf16_f32(256, g.n0);
-  const bool ok = g.n1 ? mma_k<KIND, true>(h, p, s, d0, d1, idesc0, idesc_bf16_f32(256, g.n1), t)
-                       : mma_k<KIND, false>(h, p, s, d0, d1, idesc0, idesc0, t);
+  int kb0, kb1;
+  k_range(p, ti, nk_of(h, KIND), kb0, kb1);
+  const bool ok = g.n1 ? mma_k<KIND, true>(h, p, s, d0, d1, idesc0, idesc_bf16_f32(256, g.n1), kb0, kb1, t)
+                       : mma_k<KIND, false>(h, p, s, d0, d1, idesc0, idesc0, kb0, kb1, t);
   if (!ok) return false;
   commit2_both(&p.acc_full[b]);
   s.abuf = b ^ 1;
@@ -506,18 +519,29 @@ __device__ void epi_rows(const sym_heap &h, const Pipe &p, const TileInfo &ti, u
       }
     }
   } else if (KIND == ROUTER) {
-    const int ld = h.s.num_experts;
-    const int feature = ti.f * 256 + (int)p.rank * 128 + q * 32 + lane;  // expert of this lane
-    float *out = p.logits + (size_t)row * ld + feature;
-    const bool live = feature < ld;
+    // this lane's token; columns [row, row + nrows) are router rows (experts),
+    // stored contiguously in the token's logits row
+    const int ld = h.s.num_experts, N = h.s.world * h.s.tokens_per_slot;
+    const int token = ti.f * 256 + (int)p.rank * 128 + q * 32 + lane;
+    float *out = p.logits + (size_t)ti.ks * N * ld + (size_t)token * ld + row;
+    const bool live = token < N;
+    const bool vec = (ld & 3) == 0 && (reinterpret_cast<uintptr_t>(p.logits) & 15u) == 0;
     for (int c0 = 0; c0 < nrows; c0 += 32) {
       uint32_t v[32];
       tmem_ld32(tcol + c0, v);
       tmem_ld_wait();
       if (c0 == 0) head();
+      if (!live) continue;
+      if (vec && c0 + 32 <= nrows) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (live && c0 + c < nrows) out[(size_t)(c0 + c) * ld] = __uint_as_float(v[c]);
+        for (int c = 0; c < 32; c += 4)
+          *reinterpret_cast<float4 *>(out + c0 + c) = make_float4(
+              __uint_as_float(v[c]), __uint_as_float(v[c + 1]), __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c0 + c < nrows) out[c0 + c] = __uint_as_float(v[c]);
+      }
     }
   } else {
     const int ld = h.s.hidden;

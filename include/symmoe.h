@@ -167,11 +167,27 @@ int moe_route_topk(const sym_heap *h, const float *logits, int32_t *idx, float *
  *   tensor cores, fp32 output.
  *   x: device [N][H] bf16 (16-byte aligned);  w_router: device [E][H] bf16
  *   (16-byte aligned);  logits: device [N][E] fp32.  N, H, E from the heap's
- *   shape; the heap is read for its shape and status word only.
+ *   shape.  When there are fewer output tiles than CTA pairs, K is split
+ *   across pairs: the fp32 partials go to slot 0's y window (the expert
+ *   output, which holds nothing between a combine and the next expert FFN)
+ *   and a second kernel adds them in split order, so the logits do not depend
+ *   on the schedule.  The call must therefore not overlap an expert FFN or a
+ *   combine on the same heap; it writes nothing else of the heap but the
+ *   status word.
  * Returns SYM_OK, SYM_EINVAL (pointer/alignment) or SYM_ECUDA; asynchronous.
  */
 int moe_router_logits(const sym_heap *h, const uint16_t *x, const uint16_t *w_router, float *logits,
                       symmoe_stream_t stream);
+
+/*
+ * moe_router_splits: the number of K splits moe_router_logits uses for this
+ * heap's shape on the current device (1: one GEMM launch writing the logits;
+ * S > 1: S partials in slot 0's y window and one reduction launch).  No
+ * device work; host only apart from reading the device's SM count.
+ *   splits: host int (out).
+ * Returns SYM_OK, SYM_EINVAL (bad heap or NULL splits) or SYM_ECUDA.
+ */
+int moe_router_splits(const sym_heap *h, int *splits);
 
 /*
  * moe_dispatch: the all-to-all scatter of "Zero-copy MoE dispatch".

@@ -133,6 +133,8 @@ def test_calls_reject_bad_pointers_without_device_work():
         lambda: sm.moe_expert_ffn_ex(d, A, A, A, 2, 0),      # unknown flag
         lambda: sm.moe_combine_ex(d, None, A, A, A, 2, 0),   # unknown flag
         lambda: sm.moe_combine_ex(d, None, A, None, A, 0, 0),  # weighted combine needs w
+        lambda: sm.moe_router_logits(d, A + 8, A, A, 0),     # x not 16-byte aligned
+        lambda: sm.moe_router_logits(d, A, A, A + 2, 0),     # logits not 4-byte aligned
     ]
     for c in cases:
         with pytest.raises(sm.SymmoeError) as ei:
@@ -142,6 +144,9 @@ def test_calls_reject_bad_pointers_without_device_work():
     bad.cap += 1                                              # inconsistent descriptor
     with pytest.raises(sm.SymmoeError):
         sm.moe_route_topk(bad, A, A, A, 0)
+    with pytest.raises(sm.SymmoeError) as ei:
+        sm.moe_router_splits(bad)
+    assert ei.value.code == sm.SYM_EINVAL
     assert d.epoch == 0                                       # rejected calls change nothing
 
 

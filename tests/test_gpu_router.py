@@ -45,12 +45,19 @@ def _run(sm, cfg):
 CASES = dict(SMALL)
 CASES["wide_e"] = dict(world=3, tokens_per_slot=90, hidden=256, num_experts=300, topk=4, inter=128)
 CASES["remainder"] = dict(world=2, tokens_per_slot=135, hidden=384, num_experts=8, topk=2, inter=128)
+# few tiles and a long K: K is split across pairs (5 splits of 6, 6, 6, 6, 2 blocks on 152 SMs),
+# two feature tiles and a ragged token tile
+CASES["split_wide"] = dict(world=2, tokens_per_slot=300, hidden=1664, num_experts=300, topk=4, inter=128)
+# 18 splits of 3 blocks with a last split of one block; a token tail of 8 rows
+CASES["split_tail"] = dict(world=1, tokens_per_slot=520, hidden=3328, num_experts=24, topk=2, inter=128)
 
 
 @pytest.mark.parametrize("name", list(CASES))
 def test_router_small(sm, name):
     cfg = CASES[name]
     heap, logits = _run(sm, cfg)
+    if name.startswith("split_"):
+        assert heap.router_splits() > 1, "the case is meant to split K"
     ref = oracle.router_logits(ms.x_np(cfg), ms.router_weight_np(cfg))
     got = logits.cpu().numpy()
     _check_logits(got, ref, name)
@@ -64,7 +71,8 @@ def test_router_small(sm, name):
     assert np.array_equal(idx.cpu().numpy(), ri)
 
 
-@pytest.mark.parametrize("name,rows", [("mixtral", 256), ("deepseek", 128)])
+# on 152 SMs: one GEMM writing the logits; 2 K splits; 14 K splits of 8 blocks
+@pytest.mark.parametrize("name,rows", [("mixtral", 256), ("deepseek", 128), ("decode", 128)])
 def test_router_full_size_sampled(sm, name, rows):
     cfg = ms.CONFIGS[name]
     heap, logits = _run(sm, cfg)
@@ -73,3 +81,25 @@ def test_router_full_size_sampled(sm, name, rows):
     ref = oracle.router_logits(ms.x_np(cfg, rows=pick), ms.router_weight_np(cfg))
     _check_logits(logits[torch.from_numpy(pick).to(DEV)].cpu().numpy(), ref, name)
     assert torch.isfinite(logits).all()
+
+
+def test_router_split_leaves_heap_usable(sm):
+    """The K-split partials live in slot 0's y window before dispatch: a full
+    dispatch -> expert -> combine after the router still matches the staged
+    result taken without the router."""
+    cfg = CASES["split_wide"]
+    heap, logits = _run(sm, cfg)
+    n, k, H = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"], cfg["hidden"]
+    x = ms.x_torch(cfg, DEV)
+    wg, wu, wd = ms.weights_torch(cfg, DEV)
+    idx = torch.empty((n, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((n, k), dtype=torch.float32, device=DEV)
+    out1 = torch.empty((n, H), dtype=torch.bfloat16, device=DEV)
+    heap.pipeline(logits, x, wg, wu, wd, idx, w, out1)
+    fresh = sm.SymHeap(cfg, DEV)
+    out2 = torch.empty_like(out1)
+    fresh.pipeline(logits, x, wg, wu, wd, idx, w, out2)
+    torch.cuda.synchronize()
+    assert heap.status() == 0 and fresh.status() == 0
+    assert torch.equal(out1, out2)
+
