@@ -99,13 +99,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   cluster_sync();  // barriers of both CTAs initialised before any remote arrive
   tc_fence_after();
   p.tmem_base = *tmem_base_s;
-  const int nf = nf_of(h, KIND);
+  const int nf = nf_of(h, KIND), grp = tok_group_of(h, KIND);
   const int total_tiles = tb.tokprefix[E] * nf;
   const uint32_t tmo = h.wait_timeout_us;
   auto wait = [&](const uint32_t *c, uint32_t target) { return wait_counter_geq(c, target, tmo, abort_flag); };
   // the token rows of tile t dispatched (both CTAs check the whole tile)
   auto tile_ready = [&](int t, bool block) {
-    const TileInfo ti = decode_tok(h, tb, nf, t);
+    const TileInfo ti = decode_tok(h, tb, nf, grp, t);
     return rows_ready(h, ti.d, ti.row0, ti.valid, block, wait);
   };
 
@@ -124,7 +124,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       }
       while (ready_ok && t < total_tiles && !*abort_flag) {
         if (wait_ready) fence_proxy_async();  // rows written by generic stores
-        const TileInfo ti = decode_tok(h, tb, nf, t);
+        const TileInfo ti = decode_tok(h, tb, nf, grp, t);
         const int t_next = pair_tile(i + 1, pair_id, npairs);
         bool next_ok = !wait_ready || t_next >= total_tiles;
         auto probe = [&]() {
@@ -145,14 +145,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       // ---------------------------------------------------- MMA issuer (leader)
       MmaState ms;
       for (int i = 0, t; (t = pair_tile(i, pair_id, npairs)) < total_tiles; ++i)
-        if (!mma_tile<KIND>(h, p, ms, decode_tok(h, tb, nf, t), t)) break;
+        if (!mma_tile<KIND>(h, p, ms, decode_tok(h, tb, nf, grp, t), t)) break;
     }
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = wid & 3;  // TMEM lane quarter this warp may access
     EpiState es;
     for (int i = 0, t; (t = pair_tile(i, pair_id, npairs)) < total_tiles; ++i)
-      if (!epi_tile<KIND>(h, p, es, decode_tok(h, tb, nf, t), t, q, lane)) break;
+      if (!epi_tile<KIND>(h, p, es, decode_tok(h, tb, nf, grp, t), t, q, lane)) break;
   }
 
   tc_fence_before();

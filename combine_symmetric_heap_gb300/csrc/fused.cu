@@ -747,13 +747,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
   __syncthreads();
   if (scanned) {
     const int nf1 = nf_of(h, GATE_UP), nf2 = nf_of(h, DOWN);
+    const int g1 = tok_group_of(h, GATE_UP), g2 = tok_group_of(h, DOWN);
     const int total1 = tb.tokprefix[E] * nf1, total2 = tb.tokprefix[E] * nf2;
     const uint32_t h_target = EPI_WARPS_PER_TILE * (uint32_t)nf1;
     auto wait = [&](const uint32_t *c, uint32_t target) { return wait_geq(h, c, target); };
     // inputs of a tile in place: its dispatched rows (gate/up) or every
     // gate/up feature tile of its token tile (down)
     auto inputs_ready = [&](int kind, int t, bool block) -> bool {
-      const TileInfo ti = decode_tok(h, tb, kind == GATE_UP ? nf1 : nf2, t);
+      const TileInfo ti = decode_tok(h, tb, kind == GATE_UP ? nf1 : nf2, kind == GATE_UP ? g1 : g2, t);
       if (kind == DOWN) {
         const uint32_t *c = h_ready(h) + tb.tokprefix[ti.e] + ti.n;
         return block ? wait_geq(h, c, h_target) : ld_acquire_u32(c) >= h_target;
@@ -792,8 +793,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
             if (!next_ok) next_ok = inputs_ready(kind_n, t_n, false);
           };
           ok = kind == GATE_UP
-                   ? produce_tile<GATE_UP>(h, p, ps, decode_tok(h, tb, nf1, t), &tm_g, &tm_u, tm_rx, -1, probe)
-                   : produce_tile<DOWN>(h, p, ps, decode_tok(h, tb, nf2, t), &tm_d, &tm_d, tm_h, -1, probe);
+                   ? produce_tile<GATE_UP>(h, p, ps, decode_tok(h, tb, nf1, g1, t), &tm_g, &tm_u, tm_rx, -1, probe)
+                   : produce_tile<DOWN>(h, p, ps, decode_tok(h, tb, nf2, g2, t), &tm_d, &tm_d, tm_h, -1, probe);
           if (!ok) break;
           if (has_next && !next_ok) ok = inputs_ready(kind_n, t_n, true);
           kind = kind_n;
@@ -807,8 +808,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
         MmaState ms;
         for (int kind = kind0, i = 0; valid_at(kind, i); next_of(kind, i)) {
           const int t = tile_at(i);
-          const bool ok = kind == GATE_UP ? mma_tile<GATE_UP>(h, p, ms, decode_tok(h, tb, nf1, t), -1)
-                                          : mma_tile<DOWN>(h, p, ms, decode_tok(h, tb, nf2, t), -1);
+          const bool ok = kind == GATE_UP ? mma_tile<GATE_UP>(h, p, ms, decode_tok(h, tb, nf1, g1, t), -1)
+                                          : mma_tile<DOWN>(h, p, ms, decode_tok(h, tb, nf2, g2, t), -1);
           if (!ok) break;
         }
         // after an abort the epilogue may stop before the last accumulator:
@@ -821,7 +822,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
       const int q = wid & 3;  // TMEM lane quarter this warp may access
       EpiState es;
       for (int kind = kind0, i = 0; valid_at(kind, i); next_of(kind, i)) {
-        const TileInfo ti = decode_tok(h, tb, kind == GATE_UP ? nf1 : nf2, tile_at(i));
+        const TileInfo ti = decode_tok(h, tb, kind == GATE_UP ? nf1 : nf2, kind == GATE_UP ? g1 : g2, tile_at(i));
         const bool ok = kind == GATE_UP ? epi_tile<GATE_UP>(h, p, es, ti, -1, q, lane)
                                         : epi_tile<DOWN>(h, p, es, ti, -1, q, lane);
         if (!ok) break;

@@ -150,7 +150,22 @@ __device__ inline void build_tok_tables(const sym_heap &h, const TokTables &tb) 
     }
   }
 }
-__device__ inline TileInfo decode_tok(const sym_heap &h, const TokTables &tb, int nf, int t) {
+// Token tiles per group in a kind's tile order.  Inside an expert the tiles
+// run feature tile major, so one weight tile serves all the expert's token
+// tiles back to back; but each feature tile then sweeps all the expert's token
+// rows again, and for gate/up (K = H) a heavy expert's rows (up to N rows of
+// H bf16) can outgrow L2 and be re-read from DRAM per feature tile.  So the
+// gate/up token tiles go in groups whose rows fit GROUP_B_BYTES: group by
+// group, feature tile major inside a group.  An expert whose rows fit keeps
+// one group (the plain order); the down GEMM (K = I, small rows) keeps one.
+constexpr long long GROUP_B_BYTES = 48ll << 20;
+__host__ __device__ inline int tok_group_of(const sym_heap &h, int kind) {
+  if (kind != GATE_UP) return 1 << 30;
+  const long long tile_b = (long long)BN * h.s.hidden * 2;
+  return (int)(GROUP_B_BYTES / tile_b) > 1 ? (int)(GROUP_B_BYTES / tile_b) : 1;
+}
+
+__device__ inline TileInfo decode_tok(const sym_heap &h, const TokTables &tb, int nf, int group, int t) {
   const int E = h.s.num_experts;
   const int key = t / nf;  // expert e owns tiles [tokprefix[e]*nf, tokprefix[e+1]*nf)
   int lo = 0, hi = E;
@@ -163,8 +178,14 @@ __device__ inline TileInfo decode_tok(const sym_heap &h, const TokTables &tb, in
   const int c = tb.cnt[lo];
   const int ntok = ntok_of(c);
   const int local = t - tb.tokprefix[lo] * nf;
-  ti.f = local / ntok;
-  ti.n = local % ntok;
+  // group g holds token tiles [g*G, g*G + w), w*nf tiles, feature tile major
+  // (G*nf <= ntok*nf: no overflow)
+  const int G = min(group, ntok);
+  const int g = local / (G * nf);
+  const int r = local - g * G * nf;
+  const int w = min(G, ntok - g * G);
+  ti.f = r / w;
+  ti.n = g * G + r % w;
   ti.d = lo / (E / h.s.world);
   ti.row0 = tb.roff[lo] + ti.n * BN;
   ti.valid = ti.n == ntok - 1 ? c - ti.n * BN : BN;

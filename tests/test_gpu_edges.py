@@ -153,3 +153,23 @@ def test_wide_rows(sm, fused):
         t = int(ref["tot"][d])
         assert np.array_equal(bits(heap.recv_x(d)[:t]), ref["rx"][d])   # dispatched rows, bit-exact
     assert_close(bits(out), bf16_f64(ref["out"]), "H=16384 out")
+
+
+@pytest.mark.parametrize("fused", [0, 1])
+def test_grouped_token_tiles(sm, fused):
+    """Gate/up token tiles of a heavy expert run in groups whose rows fit a
+    fixed L2 budget (48 MiB: 6 token tiles of 256 rows at H = 16384): 3000
+    rows make 12 tiles in two groups of 6, 1700 rows make groups of 6 and 1,
+    100 rows one short tile.  Every row's result must not depend on the order."""
+    counts = [3000, 1700, 100]
+    cfg = dict(world=1, tokens_per_slot=sum(counts), hidden=16384, num_experts=3, topk=1, inter=128)
+    idx = np.repeat(np.arange(len(counts)), counts).reshape(-1, 1)
+    idx = idx[np.random.default_rng(11).permutation(len(idx))]
+    w = np.ones_like(idx, dtype=np.float32)
+    heap, out, w_used = _run(sm, cfg, idx, w, fused)
+    assert heap.status() == 0
+    ref = _oracle_from_idx(cfg, idx, w_used, fresh_weight_fn(cfg, DEV))
+    assert ref["cnt"].tolist() == counts
+    t = int(ref["tot"][0])
+    assert_close(bits(heap.y(0)[:t]), ref["y_exact"][0], "grouped tiles y")
+    assert_close(bits(out), bf16_f64(ref["out"]), "grouped tiles out")
