@@ -6,7 +6,8 @@ this package.  The product path (the CUDA library and its Python binding)
 never imports it and has no CPU fallback.
 
 The oracle is a plain, slow, obviously-correct numpy implementation in fp64 of
-what the path computes (module ``oracle.moe``).  It shares no code with the
+what the path computes (module ``oracle.moe``), and of the GEMM + all-to-all
+fusion workload on the same heap (module ``oracle.linear_a2a``).  It shares no code with the
 CUDA path; both take their inputs from the seeded generator module
 ``moe_synth``.
 
@@ -31,4 +32,12 @@ from .moe import (  # noqa: F401
     combine_sum,
     pipeline,
     slot_address,
+)
+from .linear_a2a import (  # noqa: F401
+    linear,
+    linear_exact,
+    a2a_blocks,
+    gemm_a2a,
+    shard_gather,
+    a2a_gemm,
 )

@@ -361,3 +361,89 @@ def test_router_logits_matches_torch_cpu_fp32():
     t = lambda b: torch.from_numpy(oracle.bf16_bits_to_f64(b).astype(np.float32))
     ref = (t(x) @ t(wr).T).numpy()
     assert np.allclose(lg, ref, rtol=1e-5, atol=1e-6)
+
+
+# ------------------------------------------- GEMM + all-to-all (second workload)
+
+def _bf16_bits_of_ints(a):
+    """Exact bf16 bit patterns of small integers (|v| < 256)."""
+    return oracle.round_f64_to_bf16_bits(np.asarray(a, dtype=np.float64))
+
+
+def test_linear_a2a_hand_example():
+    g = _golden("linear_a2a_hand.json")
+    W, T = g["world"], g["tokens_per_slot"]
+    wb = _bf16_bits_of_ints(g["weight"])
+    r, _ = oracle.gemm_a2a(_bf16_bits_of_ints(g["x"]), wb, W, T)
+    assert [oracle.bf16_bits_to_f64(rj).tolist() for rj in r] == g["gemm_a2a"]
+    c, _ = oracle.a2a_gemm(_bf16_bits_of_ints(g["z"]), wb, W, T)
+    assert [oracle.bf16_bits_to_f64(cj).tolist() for cj in c] == g["a2a_gemm"]
+
+
+@pytest.mark.parametrize("W,T", [(1, 3), (2, 4), (4, 8), (3, 9)])
+def test_a2a_blocks_brute_force(W, T):
+    """Every (source slot, row) lands exactly once, at the place an independent
+    per-row formula gives; applying the exchange twice is the identity."""
+    B = T // W
+    labels = [np.array([[s * 1000 + r] for r in range(T)]) for s in range(W)]
+    out = oracle.a2a_blocks(labels, W)
+    seen = set()
+    for s in range(W):
+        for r in range(T):
+            j, rr = r // B, r % B               # destination slot, row inside the block
+            assert out[j][s * B + rr, 0] == s * 1000 + r
+            seen.add((j, s * B + rr))
+    assert len(seen) == W * T
+    back = oracle.a2a_blocks(out, W)
+    assert all(np.array_equal(b, l) for b, l in zip(back, labels))
+
+
+@pytest.mark.parametrize("W,T,Hs", [(1, 2, 3), (2, 3, 2), (4, 2, 1)])
+def test_shard_gather_brute_force(W, T, Hs):
+    N = W * T
+    z = np.array([[[s * 10000 + g * 10 + c for c in range(Hs)] for g in range(N)] for s in range(W)])
+    u = oracle.shard_gather(z, W, T)
+    for j in range(W):
+        assert u[j].shape == (T, W * Hs)
+        for r in range(T):
+            for col in range(W * Hs):
+                s, c = col // Hs, col % Hs      # feature col comes from slot s's shard
+                assert u[j][r, col] == s * 10000 + (j * T + r) * 10 + c
+
+
+def test_linear_integer_closed_form():
+    """Small integers: every product and sum is exact, so bf16(a W^T) equals the
+    int64 matrix product wherever it fits bf16's 8-bit significand."""
+    rng = np.random.default_rng(3)
+    a = rng.integers(-3, 4, size=(5, 16))
+    w = rng.integers(-2, 3, size=(6, 16))
+    ref = a.astype(np.int64) @ w.astype(np.int64).T
+    assert np.abs(ref).max() < 256
+    got = oracle.bf16_bits_to_f64(oracle.linear(_bf16_bits_of_ints(a), _bf16_bits_of_ints(w)))
+    assert np.array_equal(got, ref.astype(np.float64))
+
+
+def test_identity_weight_reduces_to_the_exchange():
+    """W = I: GEMM -> A2A is the row exchange of x and A2A -> GEMM is the shard
+    gather, bit for bit."""
+    cfg = dict(world=4, tokens_per_slot=8, hidden=16, num_experts=4, topk=1, inter=128)
+    W, T, H = cfg["world"], cfg["tokens_per_slot"], cfg["hidden"]
+    x = ms.x_np(cfg)
+    eye = _bf16_bits_of_ints(np.eye(H))
+    r, _ = oracle.gemm_a2a(x, eye, W, T)
+    ex = oracle.a2a_blocks([x[s * T:(s + 1) * T] for s in range(W)], W)
+    assert all(np.array_equal(a, b) for a, b in zip(r, ex))
+    z = np.stack([x[:, s * (H // W):(s + 1) * (H // W)] for s in range(W)])
+    c, _ = oracle.a2a_gemm(z, eye, W, T)
+    assert all(np.array_equal(a, x[j * T:(j + 1) * T]) for j, a in enumerate(c))
+
+
+def test_linear_against_torch():
+    """An independent library routine (torch CPU, fp32) on random bf16 data."""
+    cfg = dict(world=2, tokens_per_slot=16, hidden=64, num_experts=2, topk=1, inter=128)
+    x = ms.x_np(cfg)
+    w = ms.router_weight_np(dict(cfg, num_experts=64))
+    ref = (torch.from_numpy(oracle.bf16_bits_to_f64(x)).float()
+           @ torch.from_numpy(oracle.bf16_bits_to_f64(w)).float().T).double().numpy()
+    got = oracle.linear_exact(x, w)
+    assert np.allclose(got, ref, rtol=1e-5, atol=1e-5)
