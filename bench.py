@@ -48,6 +48,8 @@ def parse():
     p.add_argument("--experts", type=int, default=0, help="override E")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--workload", default="moe", choices=["moe", "linear_a2a"],
+                   help="linear_a2a: the GEMM + all-to-all workload on the same heap, fused vs split")
     return p.parse_args()
 
 
@@ -534,8 +536,78 @@ def run_ours(args):
     return 0
 
 
+def run_linear_a2a(args):
+    """GEMM -> A2A and A2A -> GEMM on the config's W, T, H: the fused form
+    against the split pipeline, alternating blocks of calls so both see the
+    same clocks; CUDA events on the calling stream."""
+    import torch
+    import moe_synth as ms
+    import combine_symmetric_heap_gb300 as sm
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = get_cfg(args)
+    W, T, H = cfg["world"], cfg["tokens_per_slot"], cfg["hidden"]
+    n = W * T
+    heap = sm.SymHeap(cfg, dev)
+    x = ms.x_torch(cfg, dev)
+    z = ms.shards_torch(cfg, dev)
+    w = ms.linear_weight_torch(cfg, dev)
+    stream = torch.cuda.current_stream(dev)
+    hbm, tf_burst, tf_sus, peak_src = peaks()
+    flops = 2.0 * n * H * H
+    # forms of each op: the fused one (the pages' LSA form), the split
+    # pipeline, and for A2A -> GEMM the copy-engine form (the pages' SDMA form)
+    forms = {"gemm_a2a": {"fused": lambda: heap.gemm_a2a(x, w, fused=True, stream=stream),
+                          "split": lambda: heap.gemm_a2a(x, w, fused=False, stream=stream)},
+             "a2a_gemm": {"fused": lambda: heap.a2a_gemm(z, w, fused=True, stream=stream),
+                          "split": lambda: heap.a2a_gemm(z, w, fused=False, stream=stream),
+                          "fused_copy_engines": lambda: heap.a2a_gemm(z, w, fused=True, copy_engines=True,
+                                                                      stream=stream)}}
+    steps, rounds = max(args.steps // 4, 5), 4
+    out = {}
+    with ClockSampler(local) as clk:
+        for name, fs in forms.items():
+            for call in fs.values():
+                for _ in range(max(args.warmup, 3)):
+                    call()
+            torch.cuda.synchronize()
+            times = {k: [] for k in fs}
+            for _ in range(rounds):   # alternating blocks: every form sees the same clocks
+                for k, call in fs.items():
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(steps):
+                        call()
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    times[k].append(e0.elapsed_time(e1) / steps)
+            assert heap.status(stream=stream) == 0, "device status word set"
+            med = {k: sorted(v)[rounds // 2] for k, v in times.items()}
+            tf = flops / (med["fused"] / 1e3) / 1e12
+            out[name] = {**{f"{k}_ms": v for k, v in med.items()},
+                         "speedup_pct": 100.0 * (med["split"] / med["fused"] - 1.0),
+                         "fused_tflops": tf, "frac": tf / tf_burst,
+                         "peak": f"{peak_src} bf16 burst {tf_burst} TFLOP/s",
+                         "exchange_bytes": n * H * 2}
+            if "fused_copy_engines" in med:
+                out[name]["copy_engines_speedup_pct"] = 100.0 * (med["split"] / med["fused_copy_engines"] - 1.0)
+    line = {"metric": "GEMM + all-to-all on the heap's slots: fused vs split, ms per call on 1 GB300",
+            "impl": "ours", "workload": "linear_a2a", "n_gpus": 1, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"linear {H}x{H} over W={W} slots of T={T} tokens ({args.config} shape)",
+                       "world_slots": W, "tokens_per_slot": T, "hidden": H,
+                       "steps_per_block": steps, "blocks": rounds},
+            **out, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.workload == "linear_a2a":
+        return run_linear_a2a(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
         L.moe_pipeline.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                    ctypes.c_int, _vp]
         L.sym_heap_status.argtypes = [P(SymHeapDesc), P(_i32), ctypes.c_int, _vp]
+        L.sym_gemm_a2a.argtypes = [P(SymHeapDesc), _vp, _vp, ctypes.c_int, _vp]
+        L.sym_a2a_gemm.argtypes = [P(SymHeapDesc), _vp, _vp, ctypes.c_int, _vp]
         L.moe_dispatch_layout_noalloc.argtypes = [P(MoeShape), _vp, _vp, _vp, _vp, _vp, _vp]
         L.sym_strerror.argtypes = [ctypes.c_int]
         L.sym_strerror.restype = ctypes.c_char_p
@@ -189,6 +191,25 @@ SYM_FFN_WEIGHTED_ROWS = 1
 SYM_COMBINE_UNWEIGHTED = 1
 SYM_PIPE_FUSED = 1
 SYM_PIPE_WEIGHTS_IN_FFN = 2
+SYM_LA_FUSED = 1
+SYM_LA_COPY_ENGINES = 2
+
+
+def sym_gemm_a2a(heap: SymHeapDesc, x, w, mode: int = 0, stream=None) -> None:
+    """GEMM -> all-to-all: slot s's rows of x through w, exchanged in W row
+    blocks into the y windows (mode SYM_LA_FUSED: the epilogue stores at the
+    destination; 0: GEMM, then a copy kernel)."""
+    _check(lib().sym_gemm_a2a(ctypes.byref(heap), _ptr(x), _ptr(w), int(mode), _stream(stream)),
+           "sym_gemm_a2a")
+
+
+def sym_a2a_gemm(heap: SymHeapDesc, z, w, mode: int = 0, stream=None) -> None:
+    """All-to-all -> GEMM: K-shards z [W][N][H/W] gathered per slot, then w;
+    results in the y windows (mode SYM_LA_FUSED: the GEMM reads each shard in
+    place; SYM_LA_FUSED | SYM_LA_COPY_ENGINES: copy-engine copies consumed as
+    they land; 0: a copy kernel, then the GEMM)."""
+    _check(lib().sym_a2a_gemm(ctypes.byref(heap), _ptr(z), _ptr(w), int(mode), _stream(stream)),
+           "sym_a2a_gemm")
 
 
 def moe_expert_ffn_ex(heap: SymHeapDesc, w_gate, w_up, w_down, flags: int = 0, stream=None) -> None:
@@ -326,6 +347,13 @@ class SymHeap:
     def pipeline(self, logits, x, wg, wu, wd, idx, w, out, fused=0, weights_in_ffn=False, stream=None):
         mode = (SYM_PIPE_FUSED if fused else 0) | (SYM_PIPE_WEIGHTS_IN_FFN if weights_in_ffn else 0)
         moe_pipeline(self.desc, logits, x, wg, wu, wd, idx, w, out, mode, stream)
+
+    def gemm_a2a(self, x, w, fused=False, stream=None):
+        sym_gemm_a2a(self.desc, x, w, SYM_LA_FUSED if fused else 0, stream)
+
+    def a2a_gemm(self, z, w, fused=False, copy_engines=False, stream=None):
+        mode = (SYM_LA_FUSED | (SYM_LA_COPY_ENGINES if copy_engines else 0)) if fused else 0
+        sym_a2a_gemm(self.desc, z, w, mode, stream)
 
 
 lib()  # fail loudly at import if the CUDA library is missing

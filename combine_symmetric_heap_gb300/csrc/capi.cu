@@ -25,6 +25,11 @@ cudaError_t launch_combine(const sym_heap &h, const uint16_t *expert_out, const 
 cudaError_t launch_router(const sym_heap &h, const uint16_t *x, const uint16_t *wr, float *logits,
                           int num_sms, cudaStream_t st);
 cudaError_t router_plan(const sym_heap &h, int num_sms, int *grid, int *splits, int *kb_per_split);
+cudaError_t launch_gemm_a2a(const sym_heap &h, const uint16_t *x, const uint16_t *w, int fused, int num_sms,
+                            cudaStream_t st);
+cudaError_t launch_a2a_gemm(const sym_heap &h, const uint16_t *z, const uint16_t *w, int mode, int num_sms,
+                            cudaStream_t st);
+int a2a_gemm_counters(const sym_heap &h);
 size_t fused_ctrl_bytes(const moe_shape &s);
 cudaError_t launch_fused(const sym_heap &h, const float *logits, const uint16_t *x,
                          const uint16_t *wg, const uint16_t *wu, const uint16_t *wd,
@@ -195,6 +200,26 @@ int moe_router_splits(const sym_heap *h, int *splits) {
   if (sms <= 0) return SYM_ECUDA;
   int grid, kb;
   return from_cuda(router_plan(*h, sms, &grid, splits, &kb));
+}
+
+int sym_gemm_a2a(const sym_heap *h, const uint16_t *x, const uint16_t *w, int mode, symmoe_stream_t stream) {
+  if (!heap_ok(h) || !aligned16(x) || !aligned16(w) || (mode & ~SYM_LA_FUSED) ||
+      h->s.tokens_per_slot % h->s.world != 0)
+    return SYM_EINVAL;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return SYM_ECUDA;
+  return from_cuda(launch_gemm_a2a(*h, x, w, mode & SYM_LA_FUSED, sms, (cudaStream_t)stream));
+}
+
+int sym_a2a_gemm(const sym_heap *h, const uint16_t *z, const uint16_t *w, int mode, symmoe_stream_t stream) {
+  if (!heap_ok(h) || !aligned16(z) || !aligned16(w) || (mode & ~(SYM_LA_FUSED | SYM_LA_COPY_ENGINES)) ||
+      mode == SYM_LA_COPY_ENGINES || h->s.hidden % (64 * h->s.world) != 0)
+    return SYM_EINVAL;
+  const bool engines = (mode & SYM_LA_COPY_ENGINES) != 0;
+  if (engines && (uint32_t)a2a_gemm_counters(*h) > h->num_ready) return SYM_ENOSPACE;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return SYM_ECUDA;
+  return from_cuda(launch_a2a_gemm(*h, z, w, engines ? 2 : (mode & SYM_LA_FUSED), sms, (cudaStream_t)stream));
 }
 
 int moe_dispatch(sym_heap *h, const uint16_t *x, const int32_t *idx, const float *w,

@@ -69,13 +69,16 @@ __host__ __device__ inline int box_index(int half_rows) {
 // with the roles turned: tokens on the MMA's M side (the "features", 256 per
 // pair tile) and the E router rows on the N side (the "rows" of one
 // pseudo-expert), so a small E costs a narrow MMA instead of a padded one;
-// fp32 output.
-enum Kind : int { GATE_UP = 0, DOWN = 1, ROUTER = 2 };
+// fp32 output.  LINEAR: out = x W^T with W [H][H] over one slot's token rows
+// (the GEMM + all-to-all workload), bf16 output routed by the Pipe.
+enum Kind : int { GATE_UP = 0, DOWN = 1, ROUTER = 2, LINEAR = 3 };
 
 // features per pair tile and K blocks per kind
 __host__ __device__ inline int feat_of(int kind) { return kind == GATE_UP ? 128 : 256; }
 __host__ __device__ inline int nf_of(const sym_heap &h, int kind) {
-  const int n = kind == GATE_UP ? h.s.inter : kind == DOWN ? h.s.hidden : h.s.world * h.s.tokens_per_slot;
+  const int n = kind == GATE_UP                  ? h.s.inter
+                : kind == DOWN || kind == LINEAR ? h.s.hidden
+                                                 : h.s.world * h.s.tokens_per_slot;
   return (n + feat_of(kind) - 1) / feat_of(kind);
 }
 __host__ __device__ inline int nk_of(const sym_heap &h, int kind) {
@@ -353,6 +356,20 @@ struct Pipe {
   int scale_rows;             // DOWN: y row p = bf16(recv_w[p] * acc) (weights in the epilogue)
   float *logits;              // ROUTER: the [N][E] fp32 output (split ks: its partial at ks*N*E)
   int kb_per_split = 0;       // K blocks per split of a tile (0: the whole K)
+  // LINEAR: output window (offset in a slot) and the all-to-all block (0: the
+  // rows stay in the tile's slot; B: source row r of slot d goes to slot r / B,
+  // row d*B + r % B).  shard_kb > 0: K arrives in shards of shard_kb blocks,
+  // stored shard major ([shard][T rows][H/W] in the B window, the B maps'
+  // rows running over shard*T + row); shard_wait: shard s of slot d arrives
+  // during the launch and is in place once word s of slot d's ready window
+  // is nonzero.  shard_direct: the B maps run over the owners' buffers
+  // instead, [shard][N tokens][H/W], and a tile of slot d reads its tokens
+  // d*T + row of every shard there (no copy)
+  uint64_t out_off = 0;
+  int a2a_block = 0;
+  int shard_kb = 0;
+  int shard_wait = 0;
+  int shard_direct = 0;
 };
 
 // K blocks [kb0, kb1) of tile ti
@@ -379,10 +396,32 @@ template <int KIND, bool TWO, typename Probe>
 __device__ __forceinline__ bool produce_k(const sym_heap &h, const Pipe &p, ProdState &s, int d, int arow,
                                           int r0, int r1, const CUtensorMap *ma0, const CUtensorMap *ma1,
                                           const CUtensorMap *mb0, const CUtensorMap *mb1, uint32_t tx, int t,
-                                          int kb0, int kb1, Probe &probe) {
+                                          int kb0, int kb1, const uint32_t *shard_ctr, Probe &probe) {
   const uint32_t full_leader = map_to(&p.full[0], 0);
   for (int kb = kb0; kb < kb1; ++kb) {
     if (kb == (kb0 + kb1) / 2) probe();
+    int bx = kb * BK, by0 = r0, by1 = r1, bz = d;
+    if (KIND == LINEAR && p.shard_kb) {
+      const int sh = kb / p.shard_kb;
+      if (shard_ctr && kb == sh * p.shard_kb) {
+        // this K shard is copied while the GEMM runs: wait until it is counted
+        if (!wait_counter_geq(shard_ctr + sh, 1u, p.tmo, p.abort)) {
+          *p.abort = 1;
+          raise_status(h, SYM_STATUS_TIMEOUT);
+          return false;
+        }
+        fence_proxy_async();
+      }
+      bx = (kb - sh * p.shard_kb) * BK;
+      if (p.shard_direct) {  // shard sh of the tile's tokens, read in the owner's buffer
+        by0 += d * h.s.tokens_per_slot;
+        by1 += d * h.s.tokens_per_slot;
+        bz = sh;
+      } else {
+        by0 += sh * h.s.tokens_per_slot;
+        by1 += sh * h.s.tokens_per_slot;
+      }
+    }
     if (!wait_or_stop(&p.empty[s.stage], s.phase ^ 1u, t, p.stop, p.abort, p.tmo, h)) return false;
     uint8_t *sb = p.ring + (size_t)s.stage * STAGE_BYTES;
     const uint32_t bar = full_leader + (uint32_t)(s.stage * sizeof(uint64_t));
@@ -393,8 +432,8 @@ __device__ __forceinline__ bool produce_k(const sym_heap &h, const Pipe &p, Prod
     } else {
       tma_load_2d_pair(sb, ma0, bar, kb * BK, arow);  // 128 down rows
     }
-    tma_load_3d_pair(sb + A_BYTES, mb0, bar, kb * BK, r0, d);
-    if (TWO) tma_load_3d_pair(sb + A_BYTES + B_BYTES, mb1, bar, kb * BK, r1, d);
+    tma_load_3d_pair(sb + A_BYTES, mb0, bar, bx, by0, bz);
+    if (TWO) tma_load_3d_pair(sb + A_BYTES + B_BYTES, mb1, bar, bx, by1, bz);
     ring_advance(s.stage, s.phase);
   }
   return true;
@@ -418,10 +457,13 @@ __device__ bool produce_tile(const sym_heap &h, const Pipe &p, ProdState &s, con
                                    : ti.e * h.s.hidden + ti.f * 256 + (int)p.rank * 128;
   int kb0, kb1;
   k_range(p, ti, nk_of(h, KIND), kb0, kb1);
+  // LINEAR with K shards that arrive during the launch: the tile's slot's counters
+  const uint32_t *shard_ctr =
+      KIND == LINEAR && p.shard_kb && p.shard_wait ? win<const uint32_t>(h, ti.d, h.off_ready) : nullptr;
   return g.n1 ? produce_k<KIND, true>(h, p, s, ti.d, arow, r0, r1, ma0, ma1, &mb.m[box0], &mb.m[box1], tx, t,
-                                      kb0, kb1, probe)
+                                      kb0, kb1, shard_ctr, probe)
               : produce_k<KIND, false>(h, p, s, ti.d, arow, r0, r1, ma0, ma1, &mb.m[box0], &mb.m[box1], tx,
-                                       t, kb0, kb1, probe);
+                                       t, kb0, kb1, shard_ctr, probe);
 }
 
 struct MmaState {
@@ -562,6 +604,33 @@ __device__ void epi_rows(const sym_heap &h, const Pipe &p, const TileInfo &ti, u
 #pragma unroll
         for (int c = 0; c < 32; ++c)
           if (c0 + c < nrows) out[c0 + c] = __uint_as_float(v[c]);
+      }
+    }
+  } else if (KIND == LINEAR) {
+    const int ld = h.s.hidden, B = p.a2a_block;
+    const int feature = ti.f * 256 + (int)p.rank * 128 + q * 32 + lane;
+    const bool live = feature < ld;
+    for (int c0 = 0; c0 < nrows; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tcol + c0, v);
+      tmem_ld_wait();
+      if (c0 == 0) head();
+      // destination (slot j, row rr) of source row row + c0, stepped per row
+      int j = ti.d, rr = row + c0;
+      if (B) {
+        j = rr / B;
+        rr -= j * B;
+      }
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        if (live && c0 + c < nrows) {
+          const size_t drow = B ? (size_t)ti.d * B + rr : (size_t)rr;
+          win<uint16_t>(h, j, p.out_off)[drow * ld + feature] = to_bf16(__uint_as_float(v[c]));
+        }
+        if (++rr == B) {  // never true for B = 0
+          rr = 0;
+          ++j;
+        }
       }
     }
   } else {

@@ -285,6 +285,58 @@ int moe_pipeline(sym_heap *h, const float *logits, const uint16_t *x, const uint
 int sym_heap_status(const sym_heap *h, int32_t *status, int clear, symmoe_stream_t stream);
 
 /*
+ * GEMM + all-to-all fusion, a second workload on the same heap (blog,
+ * "Examples", "GEMM + all-to-all fusion": GEMM -> A2A with the epilogue
+ * writing output tiles straight into the peers' windows; A2A -> GEMM
+ * consuming remote K-shards as they arrive, polling ready counters; each
+ * against a split pipeline).  One linear layer w [H][H] (bf16, [out][in],
+ * 16-byte aligned) is shared by the W slots; fp32 accumulation on the tensor
+ * cores, bf16 results.  mode: SYM_LA_FUSED for the fused form, 0 for the split
+ * pipeline (same results, bit for bit).  Neither call may overlap a
+ * dispatch, expert FFN or combine on the same heap (they share its windows).
+ */
+#define SYM_LA_FUSED 1
+#define SYM_LA_COPY_ENGINES 2 /* with SYM_LA_FUSED, sym_a2a_gemm only */
+
+/*
+ * sym_gemm_a2a: GEMM -> A2A.  Slot s computes Y_s = x_s w^T for its rows
+ * x_s = x[s*T, (s+1)*T), and the rows are exchanged all-to-all in W blocks of
+ * B = T/W rows: row s*B + r of slot j's y window receives Y_s[j*B + r].
+ *   x: device [N][H] bf16, 16-byte aligned.
+ *   fused: the GEMM epilogue stores each row at its destination;
+ *   split: the GEMM stores Y_s in rows [0, T) of slot s's recv_x window, then
+ *   a copy kernel exchanges the blocks.
+ * Requires T % W == 0.  Writes rows [0, T) of every y window (split: also of
+ * every recv_x window).  Returns SYM_OK, SYM_EINVAL or SYM_ECUDA; async.
+ */
+int sym_gemm_a2a(const sym_heap *h, const uint16_t *x, const uint16_t *w, int mode,
+                 symmoe_stream_t stream);
+
+/*
+ * sym_a2a_gemm: A2A -> GEMM.  Slot s holds the K-shard s (features
+ * [s*H/W, (s+1)*H/W)) of all N tokens: z [W][N][H/W] bf16, 16-byte aligned
+ * (z[s] plays slot s's window).  Slot j computes C_j = U_j w^T into rows
+ * [0, T) of its y window, U_j = its tokens j*T + r with every feature (shard s
+ * at columns [s*H/W, (s+1)*H/W)).
+ *   mode SYM_LA_FUSED: the all-to-all is the GEMM's operand loads: a tile of
+ *   slot j reads K shard s of its tokens straight from z[s] (nothing copied).
+ *   mode SYM_LA_FUSED | SYM_LA_COPY_ENGINES: slot j's recv_x window receives
+ *   its shards shard major, [W][T][H/W], by one cudaMemcpyAsync per (slot,
+ *   shard) on the copy engines from the library's side streams, each followed
+ *   by a stream write of 1 into word s of slot j's ready window; the GEMM runs
+ *   at the same time and its producer waits (bounded) for a shard's word
+ *   before it loads that K range.  A wait that expires sets
+ *   SYM_STATUS_TIMEOUT.  The call is ordered on `stream` as a whole.  Needs W
+ *   words in a ready window (SYM_ENOSPACE if the heap has fewer).
+ *   mode 0 (split): an SM copy kernel into the same shard-major blocks, then
+ *   the GEMM.
+ * Requires H % (64*W) == 0 (whole K blocks per shard).  Returns SYM_OK,
+ * SYM_EINVAL, SYM_ENOSPACE or SYM_ECUDA; async.
+ */
+int sym_a2a_gemm(const sym_heap *h, const uint16_t *z, const uint16_t *w, int mode,
+                 symmoe_stream_t stream);
+
+/*
  * moe_dispatch_layout_noalloc: the dispatch layout without a heap, for
  * callers that cannot allocate device memory (a plug-in whose host framework
  * hands it only its input and output buffers and owns every allocation, or a

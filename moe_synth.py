@@ -43,6 +43,8 @@ STREAM_WU = 4
 STREAM_WD = 5
 STREAM_PERM = 6
 STREAM_WR = 7  # router (gate) weights [E, H]
+STREAM_WL = 8  # linear layer of the GEMM + all-to-all workload [H, H]
+STREAM_Z = 9   # its K-shards [W, N, H/W]
 
 LOGIT_SIGMA = 1.0
 X_SIGMA = 1.0
@@ -200,6 +202,28 @@ def router_weight_np(cfg: dict, seed: int = 0) -> np.ndarray:
     return _chunked(lambda ix: normal_bf16_np(seed, STREAM_WR, ix, W_SIGMA), 0, e * h).reshape(e, h)
 
 
+def linear_weight_np(cfg: dict, seed: int = 0, rows: np.ndarray | None = None) -> np.ndarray:
+    """bf16 bit patterns of the linear layer W [H, H] ([out][in]), or of its
+    rows ``rows``."""
+    h = cfg["hidden"]
+    if rows is None:
+        return _chunked(lambda ix: normal_bf16_np(seed, STREAM_WL, ix, W_SIGMA), 0, h * h).reshape(h, h)
+    ix = (np.asarray(rows, dtype=np.int64)[:, None] * h + np.arange(h, dtype=np.int64)[None, :]).ravel()
+    return normal_bf16_np(seed, STREAM_WL, ix, W_SIGMA).reshape(len(rows), h)
+
+
+def shards_np(cfg: dict, seed: int = 0, tokens: np.ndarray | None = None) -> np.ndarray:
+    """bf16 bit patterns of the K-shards Z [W, N, H/W] (slot s holds features
+    [s*H/W, (s+1)*H/W) of every token), or [W, len(tokens), H/W] for the given
+    tokens only."""
+    W, T, h = cfg["world"], cfg["tokens_per_slot"], cfg["hidden"]
+    n, hs = W * T, h // W
+    tok = np.arange(n, dtype=np.int64) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    ix = ((np.arange(W, dtype=np.int64)[:, None, None] * n + tok[None, :, None]) * hs
+          + np.arange(hs, dtype=np.int64)[None, None, :]).ravel()
+    return normal_bf16_np(seed, STREAM_Z, ix, X_SIGMA).reshape(W, len(tok), hs)
+
+
 def bf16_bits_to_f32_np(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
@@ -294,6 +318,21 @@ def router_weight_torch(cfg: dict, device, seed: int = 0):
     import torch
     out = torch.empty((cfg["num_experts"], cfg["hidden"]), dtype=torch.bfloat16, device=device)
     return fill_normal_bf16_torch(out, seed, STREAM_WR, 0, W_SIGMA)
+
+
+def linear_weight_torch(cfg: dict, device, seed: int = 0):
+    """Linear layer W [H, H] bf16 on ``device`` (the bits of ``linear_weight_np``)."""
+    import torch
+    out = torch.empty((cfg["hidden"], cfg["hidden"]), dtype=torch.bfloat16, device=device)
+    return fill_normal_bf16_torch(out, seed, STREAM_WL, 0, W_SIGMA)
+
+
+def shards_torch(cfg: dict, device, seed: int = 0):
+    """K-shards Z [W, N, H/W] bf16 on ``device`` (the bits of ``shards_np``)."""
+    import torch
+    W, T, h = cfg["world"], cfg["tokens_per_slot"], cfg["hidden"]
+    out = torch.empty((W, W * T, h // W), dtype=torch.bfloat16, device=device)
+    return fill_normal_bf16_torch(out, seed, STREAM_Z, 0, X_SIGMA)
 
 
 def weights_torch(cfg: dict, device, seed: int = 0):

@@ -135,6 +135,12 @@ def test_calls_reject_bad_pointers_without_device_work():
         lambda: sm.moe_combine_ex(d, None, A, None, A, 0, 0),  # weighted combine needs w
         lambda: sm.moe_router_logits(d, A + 8, A, A, 0),     # x not 16-byte aligned
         lambda: sm.moe_router_logits(d, A, A, A + 2, 0),     # logits not 4-byte aligned
+        lambda: sm.sym_gemm_a2a(d, A + 8, A, 0, 0),          # x not 16-byte aligned
+        lambda: sm.sym_gemm_a2a(d, A, A, 2, 0),              # unknown mode bit
+        lambda: sm.sym_a2a_gemm(d, A, None, 1, 0),           # no weight
+        lambda: sm.sym_a2a_gemm(d, A, A, 4, 0),              # unknown mode bit
+        lambda: sm.sym_a2a_gemm(d, A, A, 2, 0),              # copy engines without the fused bit
+        lambda: sm.sym_gemm_a2a(d, A, A, 3, 0),              # copy engines: A2A -> GEMM only
     ]
     for c in cases:
         with pytest.raises(sm.SymmoeError) as ei:
@@ -154,3 +160,28 @@ def test_strerror():
     assert sm.sym_strerror(0) == "success"
     assert "wait" in sm.sym_strerror(sm.SYM_ETIMEOUT)
     assert sm.sym_strerror(-99).startswith("unknown")
+
+
+def test_linear_a2a_shape_rules():
+    """GEMM -> A2A needs T % W == 0; A2A -> GEMM needs whole K blocks per
+    shard (H % (64*W) == 0), and its copy-engine form W counters in a slot's
+    ready window."""
+    A = 1 << 41
+    def desc(cfg):
+        prs, total = sm.sym_heap_bytes(cfg)
+        return sm.sym_heap_init(cfg, 1 << 40, total)
+    odd_t = desc(dict(world=4, tokens_per_slot=6, hidden=256, num_experts=4, topk=1, inter=128))
+    with pytest.raises(sm.SymmoeError) as ei:
+        sm.sym_gemm_a2a(odd_t, A, A, 1, 0)
+    assert ei.value.code == sm.SYM_EINVAL
+    narrow = desc(dict(world=4, tokens_per_slot=8, hidden=128, num_experts=4, topk=1, inter=128))
+    with pytest.raises(sm.SymmoeError) as ei:
+        sm.sym_a2a_gemm(narrow, A, A, 0, 0)
+    assert ei.value.code == sm.SYM_EINVAL
+    # 2 slots x 64 tokens, k = 1: cap = 128 rows, one ready word per slot, 2 needed
+    few = desc(dict(world=2, tokens_per_slot=64, hidden=128, num_experts=2, topk=1, inter=128))
+    assert few.num_ready == 1
+    with pytest.raises(sm.SymmoeError) as ei:
+        sm.sym_a2a_gemm(few, A, A, 3, 0)
+    assert ei.value.code == sm.SYM_ENOSPACE
+

@@ -54,6 +54,18 @@ def test_whole_tensors_numpy_vs_torch_tiny_and_skew():
     assert np.array_equal(ms.logits_np(sk), ms.logits_torch(sk, "cpu").numpy())
 
 
+def test_linear_workload_inputs_numpy_vs_torch_and_slices():
+    cfg = dict(world=4, tokens_per_slot=6, hidden=256, num_experts=4, topk=1, inter=128)
+    u16 = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    w = ms.linear_weight_np(cfg)
+    assert np.array_equal(w, u16(ms.linear_weight_torch(cfg, "cpu")))
+    assert np.array_equal(ms.linear_weight_np(cfg, rows=np.array([5, 200])), w[[5, 200]])
+    z = ms.shards_np(cfg)
+    assert z.shape == (4, 24, 64)
+    assert np.array_equal(z, u16(ms.shards_torch(cfg, "cpu")))
+    assert np.array_equal(ms.shards_np(cfg, tokens=np.array([0, 17])), z[:, [0, 17]])
+
+
 def test_moments():
     v = ms.normal_f32_np(0, 2, np.arange(400000), 1.0).astype(np.float64)
     assert abs(v.mean()) < 0.01
