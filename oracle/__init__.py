@@ -25,6 +25,8 @@ from .moe import (  # noqa: F401
     count_experts,
     place_pairs,
     dispatch_rows,
+    dedup_tokens,
+    dedup_row_source,
     expert_ffn_rows,
     expert_ffn,
     combine,

@@ -157,6 +157,48 @@ def dispatch_rows(x_bits: np.ndarray, recv_pair: list, topk: int):
 
 
 # ---------------------------------------------------------------------------
+# rank-deduplicated dispatch: each token crosses to a slot once, then the
+# receiving slot expands it to its expert rows
+# ---------------------------------------------------------------------------
+
+def dedup_tokens(idx: np.ndarray, num_experts: int, world: int) -> list:
+    """Per slot d, the tokens that have at least one expert on d, in ascending
+    token order (source slot, then token): row q of slot d's staging holds
+    token dedup_tokens(...)[d][q].  The pages leave the receive layout open;
+    this is the deduplicated reading of the dispatch (one row per destination
+    slot and token instead of one per (token, k) pair)."""
+    idx = np.asarray(idx)
+    e_loc = num_experts // world
+    out = [[] for _ in range(world)]
+    for g in range(idx.shape[0]):
+        slots = sorted({int(e) // e_loc for e in idx[g]})
+        for d in slots:
+            out[d].append(g)
+    return [np.array(t, dtype=np.int64) for t in out]
+
+
+def dedup_row_source(idx: np.ndarray, num_experts: int, world: int, pos: np.ndarray) -> list:
+    """Per slot d and received row p (the expert-expanded layout of
+    place_pairs), the staging row q whose token the row copies."""
+    idx = np.asarray(idx)
+    n, k = idx.shape
+    e_loc = num_experts // world
+    toks = dedup_tokens(idx, num_experts, world)
+    q_of = [{int(g): q for q, g in enumerate(t)} for t in toks]
+    total = [0] * world
+    for g in range(n):
+        for j in range(k):
+            d = int(idx[g, j]) // e_loc
+            total[d] = max(total[d], int(pos[g, j]) + 1)
+    src = [np.full(total[d], -1, dtype=np.int64) for d in range(world)]
+    for g in range(n):
+        for j in range(k):
+            d = int(idx[g, j]) // e_loc
+            src[d][int(pos[g, j])] = q_of[d][g]
+    return src
+
+
+# ---------------------------------------------------------------------------
 # a4 + a5: SwiGLU expert on a block of received rows
 # ---------------------------------------------------------------------------
 

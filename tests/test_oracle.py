@@ -447,3 +447,54 @@ def test_linear_against_torch():
            @ torch.from_numpy(oracle.bf16_bits_to_f64(w)).float().T).double().numpy()
     got = oracle.linear_exact(x, w)
     assert np.allclose(got, ref, rtol=1e-5, atol=1e-5)
+
+
+# ------------------------------------------------ rank-deduplicated dispatch
+
+@pytest.mark.parametrize("n,E,W,k", [(6, 4, 2, 2), (9, 8, 4, 3), (5, 6, 3, 6), (7, 4, 4, 1)])
+def test_dedup_tokens_brute_force(n, E, W, k):
+    """Token g appears in slot d's staging iff one of its k experts lives on d,
+    exactly once, in ascending g; the counts equal an independent per-slot
+    set count."""
+    rng = np.random.default_rng(n * 100 + E)
+    idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(n)])
+    toks = oracle.dedup_tokens(idx, E, W)
+    e_loc = E // W
+    for d in range(W):
+        expect = [g for g in range(n) if any(int(e) // e_loc == d for e in idx[g])]
+        assert toks[d].tolist() == expect
+    # fewer rows cross than pairs, unless every token's experts sit on distinct slots
+    assert sum(len(t) for t in toks) <= n * k
+
+
+def test_dedup_expansion_reproduces_the_pair_layout():
+    """Expanding each slot's staging rows through the row sources gives the
+    expert-expanded receive rows of the plain dispatch, bit for bit."""
+    cfg = dict(ms.CONFIGS["tiny"], tokens_per_slot=16)
+    E, W, k = cfg["num_experts"], cfg["world"], cfg["topk"]
+    lg = ms.logits_np(cfg)
+    idx, w = oracle.route_topk(lg, k)
+    pos, rp, rw = oracle.place_pairs(idx, w, E, W)
+    x = ms.x_np(cfg)
+    plain = oracle.dispatch_rows(x, rp, k)
+    toks = oracle.dedup_tokens(idx, E, W)
+    src = oracle.dedup_row_source(idx, E, W, pos)
+    for d in range(W):
+        staging = x[toks[d]]
+        assert np.array_equal(staging[src[d]], plain[d])
+
+
+def test_dedup_hand_example():
+    """E = 4 on W = 2 slots (experts 0-1 on slot 0, 2-3 on slot 1), k = 2.
+    Token 0 -> experts (1, 0): twice on slot 0, so it crosses to slot 0 once;
+    token 1 -> (2, 1): once to each slot; token 2 -> (3, 2): twice on slot 1.
+    Staging: slot 0 holds tokens [0, 1], slot 1 holds [1, 2].  Pair rows of
+    slot 0 (expert 0 then 1, ascending token): e0: t0; e1: t0, t1 -> staging
+    rows [0, 0, 1]; slot 1: e2: t1, t2; e3: t2 -> staging rows [0, 1, 1]."""
+    idx = np.array([[1, 0], [2, 1], [3, 2]])
+    w = np.ones((3, 2), dtype=np.float32)
+    toks = oracle.dedup_tokens(idx, 4, 2)
+    assert [t.tolist() for t in toks] == [[0, 1], [1, 2]]
+    pos, _, _ = oracle.place_pairs(idx, w, 4, 2)
+    src = oracle.dedup_row_source(idx, 4, 2, pos)
+    assert [s.tolist() for s in src] == [[0, 0, 1], [0, 1, 1]]
