@@ -38,6 +38,8 @@ def parse():
     p.add_argument("--fused", action="store_true", help="single-launch pipeline")
     p.add_argument("--with-router", action="store_true",
                    help="start each step from the token activations: the router GEMM produces the logits")
+    p.add_argument("--dedup", action="store_true",
+                   help="rank-deduplicated dispatch (staged pipeline only)")
     p.add_argument("--weights-in-ffn", action="store_true",
                    help="routing weights applied in the expert epilogue, unweighted combine")
     p.add_argument("--unfused", action="store_true",
@@ -317,6 +319,8 @@ def run_ours(args):
     cfg = get_cfg(args)
     fused = 1 if (args.fused or (cfg.get("fused") and not args.unfused)) else 0
     wif = bool(getattr(args, "weights_in_ffn", False))
+    dedup = bool(getattr(args, "dedup", False))
+    assert not (dedup and fused), "the deduplicated dispatch runs in the staged pipeline"
     with_router = bool(getattr(args, "with_router", False))
     n, k, H = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"], cfg["hidden"]
 
@@ -352,7 +356,7 @@ def run_ours(args):
                                                weights_in_ffn=wif, stream=stream))
         else:
             calls += [lambda: heap.route_topk(logits, idx, w, stream=stream),
-                      lambda: heap.dispatch(x, idx, w, stream=stream),
+                      lambda: heap.dispatch(x, idx, w, dedup=dedup, stream=stream),
                       lambda: heap.expert_ffn(wg, wu, wd, weighted_rows=wif, stream=stream),
                       lambda: heap.combine(idx, w, out, unweighted=wif, stream=stream)]
         for j, call in enumerate(calls):
@@ -441,6 +445,14 @@ def run_ours(args):
         stage_bw["router_frac"] = max(stage_bw["router_gbs"] / hbm, stage_bw["router_tflops"] / tf_peak)
         stage_bw["router_splits"] = heap.router_splits()
 
+    if dedup:
+        # rows that cross to another slot: one per (token, distinct slot) instead of one per pair
+        import numpy as np
+        slots = np.sort(idx.cpu().numpy() // (cfg["num_experts"] // cfg["world"]), axis=1)
+        rows = int(n + (np.diff(slots, axis=1) != 0).sum())
+        stage_bw["dedup"] = {"rows_crossing": rows, "pairs": n * k, "cross_slot_bytes": rows * H * 2,
+                             "plain_cross_slot_bytes": n * k * H * 2}
+
     # ---- end to end through the public API with host buffers
     # Every step copies its inputs (logits, x) from pinned host memory and reads
     # its output back, as a serving loop does: the copies run on their own
@@ -480,7 +492,7 @@ def run_ours(args):
                 if with_router:
                     heap.router_logits(x_d[b], wr, lg_d[b], stream=stream)
                 heap.pipeline(lg_d[b], x_d[b], wg, wu, wd, idx, w, out_d[b], fused=fused, weights_in_ffn=wif,
-                              stream=stream)
+                              dedup=dedup, stream=stream)
                 computed[b] = ev()
                 computed[b].record(stream)
                 with torch.cuda.stream(s_down):
@@ -523,7 +535,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(args.config, cfg, fused, wif, with_router),
+            "config": dict(workload_config(args.config, cfg, fused, wif, with_router), dedup=dedup),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),

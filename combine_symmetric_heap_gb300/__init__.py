@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
         L.moe_router_logits.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
         L.moe_router_splits.argtypes = [P(SymHeapDesc), P(ctypes.c_int)]
         L.moe_dispatch.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
+        L.moe_dispatch_ex.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, ctypes.c_int, _vp]
         L.moe_expert_ffn.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
         L.moe_expert_ffn_ex.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, ctypes.c_int, _vp]
         L.moe_combine.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp, _vp]
@@ -191,7 +192,9 @@ SYM_FFN_WEIGHTED_ROWS = 1
 SYM_COMBINE_UNWEIGHTED = 1
 SYM_PIPE_FUSED = 1
 SYM_PIPE_WEIGHTS_IN_FFN = 2
+SYM_PIPE_DEDUP = 4
 SYM_LA_FUSED = 1
+SYM_DISPATCH_DEDUP = 1
 SYM_LA_COPY_ENGINES = 2
 
 
@@ -212,6 +215,12 @@ def sym_a2a_gemm(heap: SymHeapDesc, z, w, mode: int = 0, stream=None) -> None:
            "sym_a2a_gemm")
 
 
+def moe_dispatch_ex(heap: SymHeapDesc, x, idx, w, flags: int = 0, stream=None) -> None:
+    """flags: SYM_DISPATCH_DEDUP for the rank-deduplicated dispatch (same windows)."""
+    _check(lib().moe_dispatch_ex(ctypes.byref(heap), _ptr(x), _ptr(idx), _ptr(w), int(flags),
+                                 _stream(stream)), "moe_dispatch_ex")
+
+
 def moe_expert_ffn_ex(heap: SymHeapDesc, w_gate, w_up, w_down, flags: int = 0, stream=None) -> None:
     _check(lib().moe_expert_ffn_ex(ctypes.byref(heap), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
                                    int(flags), _stream(stream)), "moe_expert_ffn_ex")
@@ -228,7 +237,7 @@ def moe_combine_fallback_copies() -> int:
 
 def moe_pipeline(heap: SymHeapDesc, logits, x, w_gate, w_up, w_down, idx, w, out,
                  mode: int = 0, stream=None) -> None:
-    """mode: SYM_PIPE_FUSED and/or SYM_PIPE_WEIGHTS_IN_FFN bits (0: staged)."""
+    """mode: SYM_PIPE_FUSED, SYM_PIPE_WEIGHTS_IN_FFN, SYM_PIPE_DEDUP bits (0: staged)."""
     _check(lib().moe_pipeline(ctypes.byref(heap), _ptr(logits), _ptr(x), _ptr(w_gate),
                               _ptr(w_up), _ptr(w_down), _ptr(idx), _ptr(w), _ptr(out),
                               int(mode), _stream(stream)), "moe_pipeline")
@@ -334,8 +343,8 @@ class SymHeap:
     def router_splits(self) -> int:
         return moe_router_splits(self.desc)
 
-    def dispatch(self, x, idx, w, stream=None):
-        moe_dispatch(self.desc, x, idx, w, stream)
+    def dispatch(self, x, idx, w, dedup=False, stream=None):
+        moe_dispatch_ex(self.desc, x, idx, w, SYM_DISPATCH_DEDUP if dedup else 0, stream)
 
     def expert_ffn(self, wg, wu, wd, weighted_rows=False, stream=None):
         moe_expert_ffn_ex(self.desc, wg, wu, wd, SYM_FFN_WEIGHTED_ROWS if weighted_rows else 0, stream)
@@ -344,8 +353,10 @@ class SymHeap:
         moe_combine_ex(self.desc, expert_out, idx, w, out, SYM_COMBINE_UNWEIGHTED if unweighted else 0,
                        stream)
 
-    def pipeline(self, logits, x, wg, wu, wd, idx, w, out, fused=0, weights_in_ffn=False, stream=None):
-        mode = (SYM_PIPE_FUSED if fused else 0) | (SYM_PIPE_WEIGHTS_IN_FFN if weights_in_ffn else 0)
+    def pipeline(self, logits, x, wg, wu, wd, idx, w, out, fused=0, weights_in_ffn=False, dedup=False,
+                 stream=None):
+        mode = ((SYM_PIPE_FUSED if fused else 0) | (SYM_PIPE_WEIGHTS_IN_FFN if weights_in_ffn else 0)
+                | (SYM_PIPE_DEDUP if dedup else 0))
         moe_pipeline(self.desc, logits, x, wg, wu, wd, idx, w, out, mode, stream)
 
     def gemm_a2a(self, x, w, fused=False, stream=None):

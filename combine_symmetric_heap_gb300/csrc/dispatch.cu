@@ -21,6 +21,8 @@
 //   scatter one 64-thread CTA per token: x[g] is read once and stored k times
 //           (one per destination), then recv_pair / recv_w / pos are written
 //           and the ready counter of each destination row block is raised.
+#include <algorithm>
+
 #include "symmoe_dev.cuh"
 
 namespace symmoe {
@@ -203,8 +205,201 @@ __global__ void __launch_bounds__(SCATTER_THREADS)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Rank-deduplicated dispatch: a token crosses to each destination slot once,
+// into that slot's staging rows (its y window, idle until the down GEMM), and
+// the slot expands the staged rows to its expert rows locally.  The staging
+// order is ascending token g per slot; the windows the expert FFN and the
+// combine read come out bit-identical to the plain dispatch's.  Scratch in
+// the h windows (idle until the gate/up GEMM): per slot d its row sources
+// [cap] at the start of its h window; slot 0's h window also holds, after
+// that, the per-slot 32-token chunk counts [W][nch] and each pair's rank
+// among its chunk's tokens bound for the pair's slot [N][k].
+//   dedup_count    one warp per 32 tokens: per slot a ballot of the tokens
+//                  with an expert there -> counts and ranks
+//   dedup_scan     exclusive scan of each slot's chunk counts
+//   dedup_scatter  per token: x[g] read once, stored once per distinct slot
+//                  (row base + rank); every pair's receive row (the plain
+//                  layout), its metadata and its staging row
+//   dedup_expand   per slot and received row: copy the staged row, raise the
+//                  row block's ready counter
+// ---------------------------------------------------------------------------
+constexpr int DEDUP_MAX_WORLD = 32;
+
+__device__ __forceinline__ int32_t *dedup_hist(const sym_heap &h) {
+  return reinterpret_cast<int32_t *>(win<uint8_t>(h, 0, h.off_h) + h.cap * 4);
+}
+__device__ __forceinline__ int32_t *dedup_rank(const sym_heap &h, int nch) {
+  return dedup_hist(h) + (size_t)h.s.world * nch;
+}
+
+__global__ void __launch_bounds__(256) dedup_count_kernel(sym_heap h, const int32_t *__restrict__ idx) {
+  const int W = h.s.world, E_loc = h.s.num_experts / W, k = h.s.topk;
+  const int N = W * h.s.tokens_per_slot, nch = (N + 31) / 32;
+  const int lane = threadIdx.x & 31, chunk = (int)(blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
+  pdl_launch_dependents();
+  pdl_wait();  // the plain count and scan (and the routing) are done
+  if (chunk >= nch) return;
+  const int g = chunk * 32 + lane;
+  uint32_t mask = 0;
+  if (g < N)
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[(size_t)g * k + j];
+      if (e >= 0 && e < h.s.num_experts) mask |= 1u << (e / E_loc);
+    }
+  int32_t *hist = dedup_hist(h), *rank = dedup_rank(h, nch);
+  for (int d = 0; d < W; ++d) {
+    const uint32_t b = __ballot_sync(0xffffffffu, (mask >> d) & 1u);
+    if (lane == 0) hist[(size_t)d * nch + chunk] = __popc(b);
+    if (g < N)
+      for (int j = 0; j < k; ++j) {
+        const int e = idx[(size_t)g * k + j];
+        if (e >= 0 && e < h.s.num_experts && e / E_loc == d)
+          rank[(size_t)g * k + j] = __popc(b & ((1u << lane) - 1u));
+      }
+  }
+}
+
+__global__ void __launch_bounds__(1024) dedup_scan_kernel(sym_heap h) {
+  const int W = h.s.world, N = W * h.s.tokens_per_slot, nch = (N + 31) / 32;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  pdl_launch_dependents();
+  pdl_wait();
+  int32_t *hist = dedup_hist(h);
+  for (int d = wid; d < W; d += nw) {
+    int32_t *row = hist + (size_t)d * nch;
+    int carry = 0;
+    for (int c0 = 0; c0 < nch; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c < nch ? row[c] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (c < nch) row[c] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(SCATTER_THREADS)
+    dedup_scatter_kernel(sym_heap h, const uint4 *__restrict__ x, const int32_t *__restrict__ idx,
+                         const float *__restrict__ w) {
+  __shared__ uint4 *dst_s[32];  // staging row of pair j, or null when an earlier pair has its slot
+  const int E = h.s.num_experts, k = h.s.topk, T = h.s.tokens_per_slot, H = h.s.hidden;
+  const int E_loc = E / h.s.world;
+  const int N = h.s.world * T;
+  const int nchunks = (N + CHUNK - 1) / CHUNK, nch = (N + 31) / 32;
+  const int g = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nvec = H / 8;
+  const uint4 *src = x + (size_t)g * nvec;
+  pdl_launch_dependents();
+  pdl_wait();  // offsets, chunk bases and ranks
+  uint4 v[VEC];
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) {
+    const int c = tid + i * SCATTER_THREADS;
+    if (c < nvec) v[i] = __ldg(src + c);
+  }
+  if (tid < k) {
+    const int j = tid;
+    const int e = idx[(size_t)g * k + j];
+    int32_t *pos = win<int32_t>(h, g / T, h.off_pos) + (size_t)(g % T) * k;
+    uint4 *dst = nullptr;
+    int p = -1;
+    if (e >= 0 && e < E) {
+      const int d = e / E_loc, l = e % E_loc;
+      const int q = dedup_hist(h)[(size_t)d * nch + g / 32] + dedup_rank(h, nch)[(size_t)g * k + j];
+      const int rank = pos[j];
+      p = win<int32_t>(h, d, h.off_recv_off)[l] +
+          win<int32_t>(h, 0, h.off_hist)[(size_t)e * nchunks + g / CHUNK] + rank;
+      if (rank < 0 || p < 0 || (uint64_t)p >= h.cap || q < 0 || q >= N) {
+        raise_status(h, SYM_STATUS_OVERFLOW);
+        p = -1;
+      } else {
+        bool first = true;  // the first of the token's pairs on slot d carries the row
+        for (int i = 0; i < j; ++i) {
+          const int ei = idx[(size_t)g * k + i];
+          if (ei >= 0 && ei < E && ei / E_loc == d) first = false;
+        }
+        if (first) dst = win<uint4>(h, d, h.off_y) + (size_t)q * nvec;
+        win<int32_t>(h, d, h.off_h)[p] = q;  // row source for the expansion
+        win<int32_t>(h, d, h.off_recv_pair)[p] = g * k + j;
+        win<float>(h, d, h.off_recv_w)[p] = w[(size_t)g * k + j];
+      }
+    }
+    pos[j] = p;
+    dst_s[j] = dst;
+  }
+  __syncthreads();
+  for (int base = 0;;) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const int c = base + tid + i * SCATTER_THREADS;
+      if (c < nvec)
+        for (int j = 0; j < k; ++j)
+          if (dst_s[j]) dst_s[j][c] = v[i];
+    }
+    base += VEC * SCATTER_THREADS;
+    if (base >= nvec) break;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const int c = base + tid + i * SCATTER_THREADS;
+      if (c < nvec) v[i] = __ldg(src + c);
+    }
+  }
+}
+
+// grid (blocks, W): the blocks of slot blockIdx.y stride over its received
+// rows (the total is only known on the device).  Each of the 64 threads holds
+// VEC 16-byte vectors of a row between load and store (as the scatter does),
+// so a row is one round trip to memory; a staged row is read once per pair of
+// its token on the slot, so its loads stay cacheable.
+constexpr int EXPAND_BLOCKS = 4096;  // over all slots
+template <int VEC>
+__global__ void __launch_bounds__(SCATTER_THREADS) dedup_expand_kernel(sym_heap h) {
+  const int d = (int)blockIdx.y;
+  const int nvec = h.s.hidden / 8, N = h.s.world * h.s.tokens_per_slot;
+  const int tid = threadIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();  // the staged rows and the row sources
+  const int total = *win<const int32_t>(h, d, h.off_total);
+  for (int p = (int)blockIdx.x; p < total; p += (int)gridDim.x) {
+    const int q = win<const int32_t>(h, d, h.off_h)[p];
+    if (q < 0 || q >= N) {
+      if (tid == 0) raise_status(h, SYM_STATUS_OVERFLOW);
+      continue;
+    }
+    const uint4 *src = win<const uint4>(h, d, h.off_y) + (size_t)q * nvec;
+    uint4 *dst = win<uint4>(h, d, h.off_recv_x) + (size_t)p * nvec;
+    for (int base = 0; base < nvec; base += VEC * SCATTER_THREADS) {
+      uint4 v[VEC];
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const int c = base + tid + i * SCATTER_THREADS;
+        if (c < nvec) v[i] = __ldg(src + c);
+      }
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const int c = base + tid + i * SCATTER_THREADS;
+        if (c < nvec) dst[c] = v[i];
+      }
+    }
+    // every thread's stores precede the barrier; thread 0's fence is cumulative
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      atomicAdd(win<uint32_t>(h, d, h.off_ready) + p / SYM_ROWS_PER_FLAG, 1u);
+    }
+  }
+}
+
 cudaError_t launch_dispatch(const sym_heap &h, const uint16_t *x, const int32_t *idx,
-                            const float *w, cudaStream_t st) {
+                            const float *w, int dedup, cudaStream_t st) {
   const int N = h.s.world * h.s.tokens_per_slot;
   const int nchunks = (N + CHUNK - 1) / CHUNK;
   const size_t mask_bytes = (size_t)h.s.num_experts * (CHUNK / 32) * sizeof(uint32_t);
@@ -215,6 +410,24 @@ cudaError_t launch_dispatch(const sym_heap &h, const uint16_t *x, const int32_t 
   if ((err = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(1024), 0, st, h)) != cudaSuccess) return err;
   // vectors per thread: the whole row in one pass up to H = 8192
   const int nvec = h.s.hidden / 8;
+  if (dedup) {
+    const int nch = (N + 31) / 32;
+    if ((err = launch_pdl(dedup_count_kernel, dim3((nch + 7) / 8), dim3(256), 0, st, h, idx)) != cudaSuccess)
+      return err;
+    if ((err = launch_pdl(dedup_scan_kernel, dim3(1), dim3(1024), 0, st, h)) != cudaSuccess) return err;
+    auto dk = nvec <= 4 * SCATTER_THREADS   ? dedup_scatter_kernel<4>
+              : nvec <= 8 * SCATTER_THREADS ? dedup_scatter_kernel<8>
+                                            : dedup_scatter_kernel<16>;
+    if ((err = launch_pdl(dk, dim3(N), dim3(SCATTER_THREADS), 0, st, h, reinterpret_cast<const uint4 *>(x), idx,
+                          w)) != cudaSuccess)
+      return err;
+    auto ek = nvec <= 4 * SCATTER_THREADS   ? dedup_expand_kernel<4>
+              : nvec <= 8 * SCATTER_THREADS ? dedup_expand_kernel<8>
+                                            : dedup_expand_kernel<16>;
+    const unsigned per_slot =
+        (unsigned)std::max<long long>(1, std::min<long long>(EXPAND_BLOCKS / h.s.world, (long long)h.cap));
+    return launch_pdl(ek, dim3(per_slot, h.s.world), dim3(SCATTER_THREADS), 0, st, h);
+  }
   auto kern = nvec <= 4 * SCATTER_THREADS   ? dispatch_scatter_kernel<4>
               : nvec <= 8 * SCATTER_THREADS ? dispatch_scatter_kernel<8>
                                             : dispatch_scatter_kernel<16>;

@@ -204,6 +204,24 @@ int moe_dispatch(sym_heap *h, const uint16_t *x, const int32_t *idx, const float
                  symmoe_stream_t stream);
 
 /*
+ * moe_dispatch_ex: moe_dispatch with flags.  SYM_DISPATCH_DEDUP: the
+ * rank-deduplicated dispatch (a reading of "Zero-copy MoE dispatch" in which
+ * a token crosses to each destination slot once): every token row is stored
+ * once per distinct destination slot, into that slot's staging rows (its y
+ * window, rows ordered by token g; the y window holds nothing until the down
+ * GEMM), and each slot then expands its staged rows to its expert rows
+ * locally.  The windows the expert FFN and the combine read (recv_x,
+ * recv_pair, recv_w, pos, counts, offsets, ready counters) come out
+ * bit-identical to moe_dispatch's.  Scratch in the h windows (idle until the
+ * gate/up GEMM).  Needs W <= 32 and h windows of at least
+ * 4*(cap + W*ceil(N/32) + N*k) bytes (cap*I*2; true for I >= 128 and k <= 32
+ * but checked): SYM_EINVAL otherwise, or for an unknown flag.
+ */
+#define SYM_DISPATCH_DEDUP 1
+int moe_dispatch_ex(sym_heap *h, const uint16_t *x, const int32_t *idx, const float *w, int flags,
+                    symmoe_stream_t stream);
+
+/*
  * moe_expert_ffn: expert_gemm of "Zero-copy MoE dispatch", here a SwiGLU FFN
  * per expert on its received rows, in place on the heap:
  *   h = bf16(silu(recv_x Wg_e^T) * (recv_x Wu_e^T)),  y = bf16(h Wd_e^T),
@@ -267,12 +285,15 @@ uint64_t moe_combine_fallback_copies(void);
  *   SYM_PIPE_WEIGHTS_IN_FFN (2): routing weights applied in the expert
  *     epilogue and an unweighted combine (SYM_FFN_WEIGHTED_ROWS,
  *     SYM_COMBINE_UNWEIGHTED).
+ *   SYM_PIPE_DEDUP (4): the staged pipeline with the rank-deduplicated
+ *     dispatch (moe_dispatch_ex, SYM_DISPATCH_DEDUP); not with SYM_PIPE_FUSED.
  *   Any other bit: SYM_EINVAL.  mode 0 / 1 are the staged / fused pipeline.
  *   idx, w: device [N][k] outputs of the routing step; out: device [N][H].
  *   Bumps h->epoch.
  */
 #define SYM_PIPE_FUSED 1
 #define SYM_PIPE_WEIGHTS_IN_FFN 2
+#define SYM_PIPE_DEDUP 4
 int moe_pipeline(sym_heap *h, const float *logits, const uint16_t *x, const uint16_t *w_gate,
                  const uint16_t *w_up, const uint16_t *w_down, int32_t *idx, float *w,
                  uint16_t *out, int mode, symmoe_stream_t stream);

@@ -129,7 +129,8 @@ def test_calls_reject_bad_pointers_without_device_work():
         lambda: sm.moe_dispatch(d, A + 8, A, A, 0),          # x not 16-byte aligned
         lambda: sm.moe_expert_ffn(d, A, None, A, 0),
         lambda: sm.moe_combine(d, None, A, A, A + 2, 0),     # out misaligned
-        lambda: sm.moe_pipeline(d, A, A, A, A, A, A, A, A, 4, 0),  # unknown mode bit
+        lambda: sm.moe_pipeline(d, A, A, A, A, A, A, A, A, 8, 0),  # unknown mode bit
+        lambda: sm.moe_pipeline(d, A, A, A, A, A, A, A, A, 5, 0),  # dedup only staged
         lambda: sm.moe_expert_ffn_ex(d, A, A, A, 2, 0),      # unknown flag
         lambda: sm.moe_combine_ex(d, None, A, A, A, 2, 0),   # unknown flag
         lambda: sm.moe_combine_ex(d, None, A, None, A, 0, 0),  # weighted combine needs w
@@ -141,6 +142,7 @@ def test_calls_reject_bad_pointers_without_device_work():
         lambda: sm.sym_a2a_gemm(d, A, A, 4, 0),              # unknown mode bit
         lambda: sm.sym_a2a_gemm(d, A, A, 2, 0),              # copy engines without the fused bit
         lambda: sm.sym_gemm_a2a(d, A, A, 3, 0),              # copy engines: A2A -> GEMM only
+        lambda: sm.moe_dispatch_ex(d, A, A, A, 2, 0),        # unknown flag
     ]
     for c in cases:
         with pytest.raises(sm.SymmoeError) as ei:
@@ -184,4 +186,15 @@ def test_linear_a2a_shape_rules():
     with pytest.raises(sm.SymmoeError) as ei:
         sm.sym_a2a_gemm(few, A, A, 3, 0)
     assert ei.value.code == sm.SYM_ENOSPACE
+
+
+def test_dedup_dispatch_needs_at_most_32_slots():
+    A = 1 << 41
+    cfg = dict(world=64, tokens_per_slot=2, hidden=128, num_experts=64, topk=2, inter=128)
+    prs, total = sm.sym_heap_bytes(cfg)
+    d = sm.sym_heap_init(cfg, 1 << 40, total)
+    with pytest.raises(sm.SymmoeError) as ei:
+        sm.moe_dispatch_ex(d, A, A, A, sm.SYM_DISPATCH_DEDUP, 0)
+    assert ei.value.code == sm.SYM_EINVAL
+    assert d.epoch == 0
 
