@@ -27,6 +27,12 @@ from .moe import (  # noqa: F401
     dispatch_rows,
     dedup_tokens,
     dedup_row_source,
+    e4m3_decode,
+    e4m3_encode,
+    e4m3_encode_array,
+    token_scale_exp,
+    quantize_rows_e4m3,
+    dequantize_rows,
     expert_ffn_rows,
     expert_ffn,
     combine,

@@ -199,6 +199,88 @@ def dedup_row_source(idx: np.ndarray, num_experts: int, world: int, pos: np.ndar
 
 
 # ---------------------------------------------------------------------------
+# FP8 dispatch with per-token scales (the blog's dispatch carries scales,
+# recv_s): each row crosses as e4m3 codes and one scale 2^e, and the receiving
+# slot multiplies back to bf16.  Readings: OCP FP8 E4M3 (bias 7, 3 mantissa
+# bits, subnormals, largest finite 448, no infinities); the per-token scale is
+# the smallest power of two 2^e with max|x| <= 448 * 2^e (so scaling is exact
+# and only the e4m3 rounding loses bits); rounding to nearest, ties to even;
+# the dequantized value code * 2^e is exact in bf16.
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of an E4M3 code (NaN for the two NaN codes)."""
+    c = int(code) & 0xFF
+    sign = -1.0 if c & 0x80 else 1.0
+    ex, man = (c >> 3) & 0xF, c & 0x7
+    if ex == 0xF and man == 0x7:
+        return float("nan")
+    if ex == 0:
+        return sign * man * 2.0 ** -9           # subnormal: man/8 * 2^(1-7)
+    return sign * (1.0 + man / 8.0) * 2.0 ** (ex - 7)
+
+
+def e4m3_encode(v: float) -> int:
+    """Nearest E4M3 code to v (ties to the even code), saturating at +-448."""
+    v = float(v)
+    sign = 0x80 if (v < 0 or (v == 0 and np.signbit(v))) else 0
+    a = abs(v)
+    if a >= E4M3_MAX:
+        return sign | 0x7E
+    best, best_d = 0, None
+    for c in range(0x7F):                      # the 127 finite non-negative codes
+        d = abs(e4m3_decode(c) - a)
+        if best_d is None or d < best_d or (d == best_d and (c & 1) == 0 and (best & 1) == 1):
+            best, best_d = c, d
+    return sign | best
+
+
+def token_scale_exp(row_f64: np.ndarray) -> int:
+    """Smallest e with max|x| <= 448 * 2^e (0 for an all-zero row)."""
+    amax = float(np.max(np.abs(row_f64))) if row_f64.size else 0.0
+    if amax == 0.0:
+        return 0
+    e = int(np.floor(np.log2(amax / E4M3_MAX))) - 1
+    while amax > E4M3_MAX * 2.0 ** e:
+        e += 1
+    return e
+
+
+def e4m3_encode_array(v: np.ndarray) -> np.ndarray:
+    """e4m3_encode over an array: the nearest of the 127 non-negative finite
+    values (increasing with the code) by a sorted search, ties to the even
+    code, saturating at 448, sign from the input."""
+    v = np.asarray(v, dtype=np.float64)
+    table = np.array([e4m3_decode(c) for c in range(0x7F)])
+    a = np.minimum(np.abs(v), E4M3_MAX)
+    hi = np.clip(np.searchsorted(table, a, side="left"), 0, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - table[lo], table[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return code | np.where(np.signbit(v), 0x80, 0).astype(np.uint8)
+
+
+def quantize_rows_e4m3(x_bits: np.ndarray):
+    """Per row: the scale exponent e and the codes of x / 2^e."""
+    x = bf16_bits_to_f64(x_bits)
+    n, h = x.shape
+    exps = np.array([token_scale_exp(x[g]) for g in range(n)], dtype=np.int64)
+    codes = e4m3_encode_array(x * np.exp2(-exps.astype(np.float64))[:, None])
+    return codes, exps
+
+
+def dequantize_rows(codes: np.ndarray, exps: np.ndarray) -> np.ndarray:
+    """bf16 bits of code * 2^e (exact)."""
+    table = np.array([e4m3_decode(c) for c in range(256)])
+    vals = table[np.asarray(codes, dtype=np.int64)] * np.exp2(np.asarray(exps, dtype=np.float64))[:, None]
+    return round_f64_to_bf16_bits(vals)
+
+
+# ---------------------------------------------------------------------------
 # a4 + a5: SwiGLU expert on a block of received rows
 # ---------------------------------------------------------------------------
 

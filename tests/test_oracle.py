@@ -498,3 +498,61 @@ def test_dedup_hand_example():
     pos, _, _ = oracle.place_pairs(idx, w, 4, 2)
     src = oracle.dedup_row_source(idx, 4, 2, pos)
     assert [s.tolist() for s in src] == [[0, 0, 1], [0, 1, 1]]
+
+
+# ------------------------------------------------------------- FP8 dispatch
+
+def test_e4m3_table():
+    """The format's landmarks: 1.0, the largest finite 448, the smallest normal
+    2^-6 and subnormal 2^-9, -0, NaN; positive values increase with the code."""
+    d = oracle.e4m3_decode
+    assert d(0x38) == 1.0 and d(0x7E) == 448.0 and d(0x08) == 2.0 ** -6 and d(0x01) == 2.0 ** -9
+    assert d(0x00) == 0.0 and np.signbit(d(0x80)) and math.isnan(d(0x7F)) and math.isnan(d(0xFF))
+    assert d(0x77) == 240.0 and d(0x07) == 7 * 2.0 ** -9 and d(0xB8) == -1.0
+    vals = [d(c) for c in range(0x7F)]
+    assert all(a < b for a, b in zip(vals, vals[1:]))
+
+
+def test_e4m3_encode_round_trip_ties_and_saturation():
+    for c in list(range(0x7F)) + list(range(0x80, 0xFF)):
+        assert oracle.e4m3_encode(oracle.e4m3_decode(c)) == c
+    # halfway between 1.0 (0x38) and 1.125 (0x39) -> even 0x38; between 1.125 and 1.25 -> 0x3A
+    assert oracle.e4m3_encode(1.0625) == 0x38 and oracle.e4m3_encode(1.1875) == 0x3A
+    # halfway between the two smallest subnormals (2^-9, 2^-8) -> even 0x02; below half of 2^-9 -> 0
+    assert oracle.e4m3_encode(1.5 * 2.0 ** -9) == 0x02 and oracle.e4m3_encode(0.4 * 2.0 ** -9) == 0
+    assert oracle.e4m3_encode(1000.0) == 0x7E and oracle.e4m3_encode(-1000.0) == 0xFE
+    # the array form is the scalar definition
+    rng = np.random.default_rng(4)
+    v = np.concatenate([rng.normal(0, 50, 4000), rng.normal(0, 0.01, 1000), [0.0, -0.0, 448.0, 464.0]])
+    assert np.array_equal(oracle.e4m3_encode_array(v), [oracle.e4m3_encode(t) for t in v])
+
+
+def test_token_scale_is_the_smallest_power_of_two():
+    for amax, e in [(448.0, 0), (449.0, 1), (896.0, 1), (1.0, -8), (0.875, -9), (0.0, 0)]:
+        assert oracle.token_scale_exp(np.array([0.5 * amax, -amax])) == e
+    rng = np.random.default_rng(5)
+    for _ in range(50):
+        row = rng.normal(0, 10.0 ** rng.uniform(-3, 3), 64)
+        e = oracle.token_scale_exp(row)
+        m = np.max(np.abs(row)) * 2.0 ** -e
+        assert 224.0 < m <= 448.0
+
+
+def test_quantize_dequantize_exact_and_bounded():
+    """Rows already of the form code * 2^e come back bit for bit; random rows
+    within half an E4M3 step (2^-4 relative for normal codes, 2^-10 * 2^e below)."""
+    table = np.array([oracle.e4m3_decode(c) for c in range(0x7F)])
+    rng = np.random.default_rng(6)
+    exact = rng.choice(table, size=(3, 32)) * np.array([[2.0 ** 5], [2.0 ** -3], [1.0]])
+    exact[:, 0] = 448.0 * np.array([2.0 ** 5, 2.0 ** -3, 1.0])      # pins e
+    xb = oracle.round_f64_to_bf16_bits(exact)
+    codes, exps = oracle.quantize_rows_e4m3(xb)
+    assert exps.tolist() == [5, -3, 0]
+    assert np.array_equal(oracle.dequantize_rows(codes, exps), xb)
+    cfg = dict(world=2, tokens_per_slot=8, hidden=256, num_experts=2, topk=1, inter=128)
+    xb = ms.x_np(cfg)
+    codes, exps = oracle.quantize_rows_e4m3(xb)
+    x = oracle.bf16_bits_to_f64(xb)
+    back = oracle.bf16_bits_to_f64(oracle.dequantize_rows(codes, exps))
+    bound = np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * np.exp2(exps)[:, None])
+    assert np.all(np.abs(back - x) <= bound)
