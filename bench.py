@@ -40,6 +40,8 @@ def parse():
                    help="start each step from the token activations: the router GEMM produces the logits")
     p.add_argument("--dedup", action="store_true",
                    help="rank-deduplicated dispatch (staged pipeline only)")
+    p.add_argument("--fp8", action="store_true",
+                   help="FP8 dispatch with per-token scales (staged pipeline only)")
     p.add_argument("--weights-in-ffn", action="store_true",
                    help="routing weights applied in the expert epilogue, unweighted combine")
     p.add_argument("--unfused", action="store_true",
@@ -320,7 +322,9 @@ def run_ours(args):
     fused = 1 if (args.fused or (cfg.get("fused") and not args.unfused)) else 0
     wif = bool(getattr(args, "weights_in_ffn", False))
     dedup = bool(getattr(args, "dedup", False))
-    assert not (dedup and fused), "the deduplicated dispatch runs in the staged pipeline"
+    fp8 = bool(getattr(args, "fp8", False))
+    assert not ((dedup or fp8) and fused), "the deduplicated and FP8 dispatches run in the staged pipeline"
+    assert not (dedup and fp8), "one dispatch variant at a time"
     with_router = bool(getattr(args, "with_router", False))
     n, k, H = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"], cfg["hidden"]
 
@@ -356,7 +360,7 @@ def run_ours(args):
                                                weights_in_ffn=wif, stream=stream))
         else:
             calls += [lambda: heap.route_topk(logits, idx, w, stream=stream),
-                      lambda: heap.dispatch(x, idx, w, dedup=dedup, stream=stream),
+                      lambda: heap.dispatch(x, idx, w, dedup=dedup, fp8=fp8, stream=stream),
                       lambda: heap.expert_ffn(wg, wu, wd, weighted_rows=wif, stream=stream),
                       lambda: heap.combine(idx, w, out, unweighted=wif, stream=stream)]
         for j, call in enumerate(calls):
@@ -445,6 +449,9 @@ def run_ours(args):
         stage_bw["router_frac"] = max(stage_bw["router_gbs"] / hbm, stage_bw["router_tflops"] / tf_peak)
         stage_bw["router_splits"] = heap.router_splits()
 
+    if fp8:
+        # a crossing row carries H code bytes and one 4-byte scale instead of 2H bytes
+        stage_bw["fp8"] = {"cross_slot_bytes": n * k * (H + 4), "plain_cross_slot_bytes": n * k * H * 2}
     if dedup:
         # rows that cross to another slot: one per (token, distinct slot) instead of one per pair
         import numpy as np
@@ -492,7 +499,7 @@ def run_ours(args):
                 if with_router:
                     heap.router_logits(x_d[b], wr, lg_d[b], stream=stream)
                 heap.pipeline(lg_d[b], x_d[b], wg, wu, wd, idx, w, out_d[b], fused=fused, weights_in_ffn=wif,
-                              dedup=dedup, stream=stream)
+                              dedup=dedup, fp8=fp8, stream=stream)
                 computed[b] = ev()
                 computed[b].record(stream)
                 with torch.cuda.stream(s_down):
@@ -535,7 +542,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": dict(workload_config(args.config, cfg, fused, wif, with_router), dedup=dedup),
+            "config": dict(workload_config(args.config, cfg, fused, wif, with_router), dedup=dedup, fp8=fp8),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),

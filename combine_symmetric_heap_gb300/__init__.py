@@ -193,8 +193,10 @@ SYM_COMBINE_UNWEIGHTED = 1
 SYM_PIPE_FUSED = 1
 SYM_PIPE_WEIGHTS_IN_FFN = 2
 SYM_PIPE_DEDUP = 4
+SYM_PIPE_FP8 = 8
 SYM_LA_FUSED = 1
 SYM_DISPATCH_DEDUP = 1
+SYM_DISPATCH_FP8 = 2
 SYM_LA_COPY_ENGINES = 2
 
 
@@ -216,7 +218,8 @@ def sym_a2a_gemm(heap: SymHeapDesc, z, w, mode: int = 0, stream=None) -> None:
 
 
 def moe_dispatch_ex(heap: SymHeapDesc, x, idx, w, flags: int = 0, stream=None) -> None:
-    """flags: SYM_DISPATCH_DEDUP for the rank-deduplicated dispatch (same windows)."""
+    """flags: SYM_DISPATCH_DEDUP for the rank-deduplicated dispatch (same windows),
+    SYM_DISPATCH_FP8 for the FP8 dispatch with per-token scales."""
     _check(lib().moe_dispatch_ex(ctypes.byref(heap), _ptr(x), _ptr(idx), _ptr(w), int(flags),
                                  _stream(stream)), "moe_dispatch_ex")
 
@@ -343,8 +346,9 @@ class SymHeap:
     def router_splits(self) -> int:
         return moe_router_splits(self.desc)
 
-    def dispatch(self, x, idx, w, dedup=False, stream=None):
-        moe_dispatch_ex(self.desc, x, idx, w, SYM_DISPATCH_DEDUP if dedup else 0, stream)
+    def dispatch(self, x, idx, w, dedup=False, fp8=False, stream=None):
+        moe_dispatch_ex(self.desc, x, idx, w,
+                        (SYM_DISPATCH_DEDUP if dedup else 0) | (SYM_DISPATCH_FP8 if fp8 else 0), stream)
 
     def expert_ffn(self, wg, wu, wd, weighted_rows=False, stream=None):
         moe_expert_ffn_ex(self.desc, wg, wu, wd, SYM_FFN_WEIGHTED_ROWS if weighted_rows else 0, stream)
@@ -354,9 +358,9 @@ class SymHeap:
                        stream)
 
     def pipeline(self, logits, x, wg, wu, wd, idx, w, out, fused=0, weights_in_ffn=False, dedup=False,
-                 stream=None):
+                 fp8=False, stream=None):
         mode = ((SYM_PIPE_FUSED if fused else 0) | (SYM_PIPE_WEIGHTS_IN_FFN if weights_in_ffn else 0)
-                | (SYM_PIPE_DEDUP if dedup else 0))
+                | (SYM_PIPE_DEDUP if dedup else 0) | (SYM_PIPE_FP8 if fp8 else 0))
         moe_pipeline(self.desc, logits, x, wg, wu, wd, idx, w, out, mode, stream)
 
     def gemm_a2a(self, x, w, fused=False, stream=None):

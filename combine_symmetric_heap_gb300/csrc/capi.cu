@@ -16,7 +16,7 @@ namespace symmoe {
 cudaError_t launch_route_topk(const sym_heap &h, const float *logits, int32_t *idx, float *w,
                               cudaStream_t st);
 cudaError_t launch_dispatch(const sym_heap &h, const uint16_t *x, const int32_t *idx,
-                            const float *w, int dedup, cudaStream_t st);
+                            const float *w, int mode, cudaStream_t st);
 cudaError_t launch_expert_ffn(const sym_heap &h, const uint16_t *wg, const uint16_t *wu,
                               const uint16_t *wd, int num_sms, int wait_ready, int scale_rows,
                               cudaStream_t st);
@@ -238,12 +238,13 @@ static bool dedup_fits(const sym_heap *h) {
 
 int moe_dispatch_ex(sym_heap *h, const uint16_t *x, const int32_t *idx, const float *w, int flags,
                     symmoe_stream_t stream) {
-  if (!heap_ok(h) || !aligned16(x) || !aligned4(idx) || !aligned4(w) || (flags & ~SYM_DISPATCH_DEDUP))
+  if (!heap_ok(h) || !aligned16(x) || !aligned4(idx) || !aligned4(w) ||
+      (flags & ~(SYM_DISPATCH_DEDUP | SYM_DISPATCH_FP8)) || flags == (SYM_DISPATCH_DEDUP | SYM_DISPATCH_FP8))
     return SYM_EINVAL;
-  const int dedup = (flags & SYM_DISPATCH_DEDUP) ? 1 : 0;
-  if (dedup && !dedup_fits(h)) return SYM_EINVAL;
+  const int mode = (flags & SYM_DISPATCH_FP8) ? 2 : (flags & SYM_DISPATCH_DEDUP) ? 1 : 0;
+  if (mode == 1 && !dedup_fits(h)) return SYM_EINVAL;
   h->epoch += 1;
-  return from_cuda(launch_dispatch(*h, x, idx, w, dedup, (cudaStream_t)stream));
+  return from_cuda(launch_dispatch(*h, x, idx, w, mode, (cudaStream_t)stream));
 }
 
 int moe_expert_ffn_ex(const sym_heap *h, const uint16_t *w_gate, const uint16_t *w_up,
@@ -292,10 +293,12 @@ int moe_pipeline(sym_heap *h, const float *logits, const uint16_t *x, const uint
                  uint16_t *out, int mode, symmoe_stream_t stream) {
   if (!heap_ok(h) || !aligned4(logits) || !aligned16(x) || !aligned16(w_gate) ||
       !aligned16(w_up) || !aligned16(w_down) || !aligned4(idx) || !aligned4(w) ||
-      !aligned16(out) || (mode & ~(SYM_PIPE_FUSED | SYM_PIPE_WEIGHTS_IN_FFN | SYM_PIPE_DEDUP)))
+      !aligned16(out) || (mode & ~(SYM_PIPE_FUSED | SYM_PIPE_WEIGHTS_IN_FFN | SYM_PIPE_DEDUP | SYM_PIPE_FP8)))
     return SYM_EINVAL;
-  const int dedup = (mode & SYM_PIPE_DEDUP) ? 1 : 0;
-  if (dedup && ((mode & SYM_PIPE_FUSED) || !dedup_fits(h))) return SYM_EINVAL;
+  const int dmode = (mode & SYM_PIPE_FP8) ? 2 : (mode & SYM_PIPE_DEDUP) ? 1 : 0;
+  if (dmode && ((mode & SYM_PIPE_FUSED) || ((mode & SYM_PIPE_DEDUP) && (mode & SYM_PIPE_FP8)) ||
+                (dmode == 1 && !dedup_fits(h))))
+    return SYM_EINVAL;
   const cudaStream_t st = (cudaStream_t)stream;
   const int sms = num_sms_of_current_device();
   if (sms <= 0) return SYM_ECUDA;
@@ -304,7 +307,7 @@ int moe_pipeline(sym_heap *h, const float *logits, const uint16_t *x, const uint
   if (mode & SYM_PIPE_FUSED)
     return from_cuda(launch_fused(*h, logits, x, w_gate, w_up, w_down, idx, w, out, weighted, sms, st));
   cudaError_t e = launch_route_topk(*h, logits, idx, w, st);
-  if (e == cudaSuccess) e = launch_dispatch(*h, x, idx, w, dedup, st);
+  if (e == cudaSuccess) e = launch_dispatch(*h, x, idx, w, dmode, st);
   if (e == cudaSuccess) e = launch_expert_ffn(*h, w_gate, w_up, w_down, sms, 1, weighted, st);
   if (e == cudaSuccess) e = launch_combine(*h, nullptr, idx, w, out, weighted, sms, st);
   return from_cuda(e);

@@ -21,6 +21,8 @@
 //   scatter one 64-thread CTA per token: x[g] is read once and stored k times
 //           (one per destination), then recv_pair / recv_w / pos are written
 //           and the ready counter of each destination row block is raised.
+#include <cuda_fp16.h>
+
 #include <algorithm>
 
 #include "symmoe_dev.cuh"
@@ -398,8 +400,164 @@ __global__ void __launch_bounds__(SCATTER_THREADS) dedup_expand_kernel(sym_heap 
   }
 }
 
+// ---------------------------------------------------------------------------
+// FP8 dispatch with per-token scales: each row crosses as E4M3 codes (H bytes
+// instead of 2H) and one scale 2^e, the smallest power of two with
+// max|x| <= 448 * 2^e, so that x / 2^e is exact and only the E4M3 rounding
+// (to nearest, ties to even) loses bits.  The codes of pair row p go to row p
+// of the destination slot's staging (its y window, H bytes a row), the scale
+// to word p of its h window; the slot then multiplies back to bf16 (exact:
+// a code has 4 significant bits) into recv_x and raises the ready counters.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint16_t e4m3x2_rn(float lo, float hi) {
+  uint16_t r;  // upper byte from the first operand
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t c) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
+  return r;
+}
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+template <int VEC>
+__global__ void __launch_bounds__(SCATTER_THREADS)
+    fp8_scatter_kernel(sym_heap h, const uint4 *__restrict__ x, const int32_t *__restrict__ idx,
+                       const float *__restrict__ w) {
+  __shared__ uint2 *dst_s[32];
+  __shared__ int32_t slot_s[32], row_s[32];
+  __shared__ uint32_t amax_s[SCATTER_THREADS / 32];
+  const int E = h.s.num_experts, k = h.s.topk, T = h.s.tokens_per_slot, H = h.s.hidden;
+  const int E_loc = E / h.s.world;
+  const int N = h.s.world * T;
+  const int nchunks = (N + CHUNK - 1) / CHUNK;
+  const int g = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nvec = H / 8;  // 16-byte bf16 vectors; each becomes 8 code bytes
+  const uint4 *src = x + (size_t)g * nvec;
+  pdl_launch_dependents();
+  pdl_wait();
+  // pass 1: the row's largest magnitude (bf16 magnitudes order as integers)
+  uint32_t am = 0;
+  for (int c = tid; c < nvec; c += SCATTER_THREADS) {
+    const uint4 v = __ldg(src + c);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) am = max(am, max(u[i] & 0x7FFFu, (u[i] >> 16) & 0x7FFFu));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, off));
+  if ((tid & 31) == 0) amax_s[tid >> 5] = am;
+  if (tid < k) {
+    const int j = tid;
+    const int e = idx[(size_t)g * k + j];
+    int32_t *pos = win<int32_t>(h, g / T, h.off_pos) + (size_t)(g % T) * k;
+    uint2 *dst = nullptr;
+    int p = -1;
+    if (e >= 0 && e < E) {
+      const int d = e / E_loc, l = e % E_loc;
+      const int rank = pos[j];
+      p = win<int32_t>(h, d, h.off_recv_off)[l] +
+          win<int32_t>(h, 0, h.off_hist)[(size_t)e * nchunks + g / CHUNK] + rank;
+      if (rank < 0 || p < 0 || (uint64_t)p >= h.cap) {
+        raise_status(h, SYM_STATUS_OVERFLOW);
+        p = -1;
+      } else {
+        dst = reinterpret_cast<uint2 *>(win<uint8_t>(h, d, h.off_y) + (size_t)p * H);
+        win<int32_t>(h, d, h.off_recv_pair)[p] = g * k + j;
+        win<float>(h, d, h.off_recv_w)[p] = w[(size_t)g * k + j];
+      }
+    }
+    pos[j] = p;
+    dst_s[j] = dst;
+    slot_s[j] = e >= 0 && e < E ? e / E_loc : -1;
+    row_s[j] = p;
+  }
+  __syncthreads();
+  // the scale: amax = m * 2^ex with m in [0.5, 1); 448 = 0.875 * 2^9
+  int ex = 0;
+  const float amax = bf16_bits_to_float(max(amax_s[0], amax_s[1]));
+  const float m = frexpf(amax, &ex);
+  const int es = amax == 0.f ? 0 : (m <= 0.875f ? ex - 9 : ex - 8);
+  if (tid < k && dst_s[tid]) win<float>(h, slot_s[tid], h.off_h)[row_s[tid]] = ldexpf(1.f, es);
+  // pass 2: codes of x / 2^es, 8 bytes per 16-byte vector, to every destination
+  for (int base = 0; base < nvec; base += VEC * SCATTER_THREADS) {
+    uint2 q[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const int c = base + tid + i * SCATTER_THREADS;
+      if (c < nvec) {
+        const uint4 v = __ldg(src + c);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        uint16_t r[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          r[t] = e4m3x2_rn(ldexpf(bf16_bits_to_float(u[t] & 0xFFFFu), -es),
+                           ldexpf(bf16_bits_to_float(u[t] >> 16), -es));
+        q[i] = make_uint2((uint32_t)r[0] | ((uint32_t)r[1] << 16), (uint32_t)r[2] | ((uint32_t)r[3] << 16));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const int c = base + tid + i * SCATTER_THREADS;
+      if (c < nvec)
+        for (int j = 0; j < k; ++j)
+          if (dst_s[j]) dst_s[j][c] = q[i];
+    }
+  }
+}
+
+// grid (blocks, W): the blocks of slot blockIdx.y stride over its received
+// rows: bf16 row p = codes of staging row p times its scale (exact), then the
+// row block's ready counter
+template <int VEC>
+__global__ void __launch_bounds__(SCATTER_THREADS) fp8_dequant_kernel(sym_heap h) {
+  const int d = (int)blockIdx.y;
+  const int H = h.s.hidden, nvec = H / 8;
+  const int tid = threadIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();  // the codes and the scales
+  const int total = *win<const int32_t>(h, d, h.off_total);
+  for (int p = (int)blockIdx.x; p < total; p += (int)gridDim.x) {
+    const float sc = win<const float>(h, d, h.off_h)[p];
+    const uint2 *src = reinterpret_cast<const uint2 *>(win<const uint8_t>(h, d, h.off_y) + (size_t)p * H);
+    uint4 *dst = win<uint4>(h, d, h.off_recv_x) + (size_t)p * nvec;
+    for (int base = 0; base < nvec; base += VEC * SCATTER_THREADS) {
+      uint2 q[VEC];
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const int c = base + tid + i * SCATTER_THREADS;
+        if (c < nvec) q[i] = src[c];
+      }
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const int c = base + tid + i * SCATTER_THREADS;
+        if (c < nvec) {
+          const uint32_t words[2] = {q[i].x, q[i].y};
+          uint32_t o[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const uint32_t f2 = e4m3x2_to_f16x2((uint16_t)(words[t >> 1] >> ((t & 1) * 16)));
+            const float lo = __half2float(__ushort_as_half((unsigned short)(f2 & 0xFFFFu))) * sc;
+            const float hi = __half2float(__ushort_as_half((unsigned short)(f2 >> 16))) * sc;
+            // exact in bf16: the upper 16 bits of the fp32 value
+            o[t] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+          }
+          dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      atomicAdd(win<uint32_t>(h, d, h.off_ready) + p / SYM_ROWS_PER_FLAG, 1u);
+    }
+  }
+}
+
 cudaError_t launch_dispatch(const sym_heap &h, const uint16_t *x, const int32_t *idx,
-                            const float *w, int dedup, cudaStream_t st) {
+                            const float *w, int mode, cudaStream_t st) {
   const int N = h.s.world * h.s.tokens_per_slot;
   const int nchunks = (N + CHUNK - 1) / CHUNK;
   const size_t mask_bytes = (size_t)h.s.num_experts * (CHUNK / 32) * sizeof(uint32_t);
@@ -410,7 +568,21 @@ cudaError_t launch_dispatch(const sym_heap &h, const uint16_t *x, const int32_t 
   if ((err = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(1024), 0, st, h)) != cudaSuccess) return err;
   // vectors per thread: the whole row in one pass up to H = 8192
   const int nvec = h.s.hidden / 8;
-  if (dedup) {
+  if (mode == 2) {
+    auto fk = nvec <= 4 * SCATTER_THREADS   ? fp8_scatter_kernel<4>
+              : nvec <= 8 * SCATTER_THREADS ? fp8_scatter_kernel<8>
+                                            : fp8_scatter_kernel<16>;
+    if ((err = launch_pdl(fk, dim3(N), dim3(SCATTER_THREADS), 0, st, h, reinterpret_cast<const uint4 *>(x), idx,
+                          w)) != cudaSuccess)
+      return err;
+    auto qk = nvec <= 4 * SCATTER_THREADS   ? fp8_dequant_kernel<4>
+              : nvec <= 8 * SCATTER_THREADS ? fp8_dequant_kernel<8>
+                                            : fp8_dequant_kernel<16>;
+    const unsigned per_slot =
+        (unsigned)std::max<long long>(1, std::min<long long>(EXPAND_BLOCKS / h.s.world, (long long)h.cap));
+    return launch_pdl(qk, dim3(per_slot, h.s.world), dim3(SCATTER_THREADS), 0, st, h);
+  }
+  if (mode == 1) {
     const int nch = (N + 31) / 32;
     if ((err = launch_pdl(dedup_count_kernel, dim3((nch + 7) / 8), dim3(256), 0, st, h, idx)) != cudaSuccess)
       return err;

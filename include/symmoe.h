@@ -218,6 +218,18 @@ int moe_dispatch(sym_heap *h, const uint16_t *x, const int32_t *idx, const float
  * but checked): SYM_EINVAL otherwise, or for an unknown flag.
  */
 #define SYM_DISPATCH_DEDUP 1
+/*
+ * SYM_DISPATCH_FP8: the FP8 dispatch with per-token scales (the blog's
+ * dispatch carries scales, recv_s).  Each row crosses as OCP E4M3 codes (H
+ * bytes instead of 2H) with one scale 2^e per token, the smallest power of
+ * two with max|x| <= 448 * 2^e (so x / 2^e is exact; the codes round to
+ * nearest, ties to even).  The codes of pair row p land in row p of the
+ * destination slot's y window (H bytes a row), the scale in word p of its h
+ * window (fp32); the slot multiplies back to bf16 (exact) into recv_x.  The
+ * expert FFN then sees the dequantized rows: results differ from the bf16
+ * dispatch by the E4M3 rounding of x.  Not with SYM_DISPATCH_DEDUP.
+ */
+#define SYM_DISPATCH_FP8 2
 int moe_dispatch_ex(sym_heap *h, const uint16_t *x, const int32_t *idx, const float *w, int flags,
                     symmoe_stream_t stream);
 
@@ -287,6 +299,8 @@ uint64_t moe_combine_fallback_copies(void);
  *     SYM_COMBINE_UNWEIGHTED).
  *   SYM_PIPE_DEDUP (4): the staged pipeline with the rank-deduplicated
  *     dispatch (moe_dispatch_ex, SYM_DISPATCH_DEDUP); not with SYM_PIPE_FUSED.
+ *   SYM_PIPE_FP8 (8): the staged pipeline with the FP8 dispatch
+ *     (SYM_DISPATCH_FP8); not with SYM_PIPE_FUSED or SYM_PIPE_DEDUP.
  *   Any other bit: SYM_EINVAL.  mode 0 / 1 are the staged / fused pipeline.
  *   idx, w: device [N][k] outputs of the routing step; out: device [N][H].
  *   Bumps h->epoch.
@@ -294,6 +308,7 @@ uint64_t moe_combine_fallback_copies(void);
 #define SYM_PIPE_FUSED 1
 #define SYM_PIPE_WEIGHTS_IN_FFN 2
 #define SYM_PIPE_DEDUP 4
+#define SYM_PIPE_FP8 8
 int moe_pipeline(sym_heap *h, const float *logits, const uint16_t *x, const uint16_t *w_gate,
                  const uint16_t *w_up, const uint16_t *w_down, int32_t *idx, float *w,
                  uint16_t *out, int mode, symmoe_stream_t stream);

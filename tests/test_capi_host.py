@@ -129,7 +129,7 @@ def test_calls_reject_bad_pointers_without_device_work():
         lambda: sm.moe_dispatch(d, A + 8, A, A, 0),          # x not 16-byte aligned
         lambda: sm.moe_expert_ffn(d, A, None, A, 0),
         lambda: sm.moe_combine(d, None, A, A, A + 2, 0),     # out misaligned
-        lambda: sm.moe_pipeline(d, A, A, A, A, A, A, A, A, 8, 0),  # unknown mode bit
+        lambda: sm.moe_pipeline(d, A, A, A, A, A, A, A, A, 16, 0),  # unknown mode bit
         lambda: sm.moe_pipeline(d, A, A, A, A, A, A, A, A, 5, 0),  # dedup only staged
         lambda: sm.moe_expert_ffn_ex(d, A, A, A, 2, 0),      # unknown flag
         lambda: sm.moe_combine_ex(d, None, A, A, A, 2, 0),   # unknown flag
@@ -142,7 +142,10 @@ def test_calls_reject_bad_pointers_without_device_work():
         lambda: sm.sym_a2a_gemm(d, A, A, 4, 0),              # unknown mode bit
         lambda: sm.sym_a2a_gemm(d, A, A, 2, 0),              # copy engines without the fused bit
         lambda: sm.sym_gemm_a2a(d, A, A, 3, 0),              # copy engines: A2A -> GEMM only
-        lambda: sm.moe_dispatch_ex(d, A, A, A, 2, 0),        # unknown flag
+        lambda: sm.moe_dispatch_ex(d, A, A, A, 4, 0),        # unknown flag
+        lambda: sm.moe_dispatch_ex(d, A, A, A, 3, 0),        # deduplicated and FP8 together
+        lambda: sm.moe_pipeline(d, A, A, A, A, A, A, A, A, 9, 0),   # FP8 only staged
+        lambda: sm.moe_pipeline(d, A, A, A, A, A, A, A, A, 12, 0),  # deduplicated and FP8 together
     ]
     for c in cases:
         with pytest.raises(sm.SymmoeError) as ei:
