@@ -184,15 +184,19 @@ def sources_sha256(files=TRAFFIC_SOURCES) -> str:
     return hsh.hexdigest()
 
 
-def traffic_record():
+def traffic_record(workload: str, cfg: dict):
     """Per-step DRAM bytes of the expert FFN launches from the committed ncu
-    summary, or None if any of their sources changed since it was captured."""
+    summary, or None if it was captured for another workload or shape, or any
+    of its sources changed since."""
+    import moe_synth as ms
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
         rec = json.load(open(path))
         if rec.get("sources_sha256") != sources_sha256():
+            return None
+        if rec.get("workload") != workload or cfg != ms.CONFIGS.get(workload):
             return None
         return rec.get("traffic_bytes_per_step")
     except Exception:
@@ -426,7 +430,7 @@ def run_ours(args):
         other = {"tflops": alg["ffn_flops"] / kern_s / 1e12, "tensor_peak": tf_peak}
     other["frac"] = (other.get("hbm_gbs", 0) / hbm) if bound == "tensor" else other["tflops"] / tf_peak
     roofline = {"bound": bound, "kernel": kname, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": None if fused else traffic_record(),
+                "frac": achieved / peak, "traffic": None if fused else traffic_record(args.config, cfg),
                 "peak_kind": f"{peak_src} " + ("bf16 " + ("sustained" if long_region else "burst")
                                                if bound == "tensor" else "HBM copy"),
                 "algorithmic_per_step": {"flops": alg["ffn_flops"], "bytes": alg["ffn_bytes"] + extra_bytes,
