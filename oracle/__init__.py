@@ -6,14 +6,15 @@ this package.  The product path (the CUDA library and its Python binding)
 never imports it and has no CPU fallback.
 
 The oracle is a plain, slow, obviously-correct numpy implementation in fp64 of
-what the path computes (module ``oracle.moe``), and of the GEMM + all-to-all
-fusion workload on the same heap (module ``oracle.linear_a2a``).  It shares no code with the
-CUDA path; both take their inputs from the seeded generator module
-``moe_synth``.
+what the path computes (module ``oracle.moe``: routing, placement, the plain,
+deduplicated and FP8 dispatch layouts, the SwiGLU expert, the combine, the
+router GEMM), and of the GEMM + all-to-all workload on the same heap (module
+``oracle.linear_a2a``).  It shares no code with the CUDA path; both take their
+inputs from the seeded generator module ``moe_synth``.
 
-Parity pins: every function here is pinned by ``tests/test_oracle_*.py``
-against brute force on tiny inputs, closed forms, invariants and a
-hand-worked example under ``tests/golden/``.  The end-to-end float values have
+Parity pins: every function here is pinned by ``tests/test_oracle.py``
+against brute force on tiny inputs, closed forms, invariants, an independent
+library routine (torch CPU) and hand-worked examples under ``tests/golden/``.  The end-to-end float values have
 no printed worked example in the source pages, so beyond those closed forms
 and invariants their absolute values are parity-unpinned.
 """
