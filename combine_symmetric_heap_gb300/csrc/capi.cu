@@ -328,7 +328,7 @@ const char *sym_strerror(int code) {
   switch (code) {
     case SYM_OK: return "success";
     case SYM_EINVAL: return "invalid shape, pointer, alignment or argument";
-    case SYM_ENOSPACE: return "heap smaller than sym_heap_bytes() requires";
+    case SYM_ENOSPACE: return "heap (or a window of it) too small for the call";
     case SYM_ECUDA: return "CUDA runtime call or kernel launch failed";
     case SYM_ETIMEOUT: return "a bounded device wait expired";
     case SYM_EOVERFLOW: return "a row or expert index out of range";

@@ -14,6 +14,8 @@
  *     combine_in view), and combine gathers those rows back, weighted;
  *   - section "Mega-MoE: mega-kernel co-design with FlyDSL": dispatch, expert
  *     GEMM and combine fused into one kernel launch;
+ *   - section "GEMM + all-to-all fusion": GEMM -> A2A and A2A -> GEMM on the
+ *     same windows (sym_gemm_a2a, sym_a2a_gemm);
  * and the "MORI CCO Guide", sections "1. Concepts" (device communicator
  * passed by value into kernels) and "3. Memory and Windows" (collective
  * registration at identical offsets).
@@ -26,7 +28,10 @@
  *   - All pointers named dev_* or documented as device pointers must point to
  *     device memory of the current CUDA device; the library never allocates,
  *     frees or copies to/from host memory except in sym_heap_status (which
- *     reads one status word) -- the caller owns every buffer.
+ *     reads one status word) -- the caller owns every buffer.  The library's
+ *     own resources are a static device array (moe_dispatch_layout_noalloc)
+ *     and, for sym_a2a_gemm's copy-engine form, two side streams and three
+ *     events per device, created on first use and kept for the process.
  *   - bf16 tensors are passed as uint16_t bit patterns, row-major, contiguous.
  *   - All compute calls are asynchronous on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) and never synchronise the host.
@@ -56,7 +61,7 @@ typedef struct CUstream_st *symmoe_stream_t; /* == cudaStream_t */
 /* ---- status codes -------------------------------------------------------- */
 #define SYM_OK 0
 #define SYM_EINVAL (-1)    /* bad shape, pointer, alignment or argument        */
-#define SYM_ENOSPACE (-2)  /* heap smaller than sym_heap_bytes() requires      */
+#define SYM_ENOSPACE (-2)  /* heap (or a window of it) too small for the call  */
 #define SYM_ECUDA (-3)     /* a CUDA runtime call or kernel launch failed      */
 #define SYM_ETIMEOUT (-4)  /* (status word) a bounded device wait expired      */
 #define SYM_EOVERFLOW (-5) /* (status word) a row index beyond its window      */
