@@ -173,3 +173,53 @@ def test_grouped_token_tiles(sm, fused):
     t = int(ref["tot"][0])
     assert_close(bits(heap.y(0)[:t]), ref["y_exact"][0], "grouped tiles y")
     assert_close(bits(out), bf16_f64(ref["out"]), "grouped tiles out")
+
+
+@pytest.mark.parametrize("fused", [0, 1])
+@pytest.mark.parametrize("hidden,inter", [(65536, 128), (128, 65536)])
+def test_largest_hidden_and_inter(sm, fused, hidden, inter):
+    """The ABI's largest H and I: a dispatched / combined row of 8192 16-byte
+    vectors (several passes of every copy loop) and K loops of 1024 blocks in
+    the gate/up (H) or down (I) GEMM.  At H = 65536 the gate/up weights are
+    scaled by 2^-3 (exact in bf16; about the 1/sqrt(H) of a trained layer):
+    with sigma = 0.02 the gate and up values reach |h| ~ 200, where one bf16
+    step of h is 1.0, and the tensor cores' fp32 accumulation over 4096 MMAs
+    (its additions truncate) moves 0.02% of y past the per-element tolerance;
+    a truncating-accumulator model of the same inputs gives the same count."""
+    cfg = dict(world=2, tokens_per_slot=40, hidden=hidden, num_experts=2, topk=1, inter=inter)
+    scale = 2.0 ** -3 if hidden >= 65536 else 1.0
+    n, k = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"]
+    lg = ms.logits_np(cfg)
+    idx_np, w_np = oracle.route_topk(lg, k)
+    heap = sm.SymHeap(cfg, DEV)
+    x = ms.x_torch(cfg, DEV)
+    wg, wu, wd = ms.weights_torch(cfg, DEV)
+    wg.mul_(scale)
+    wu.mul_(scale)
+    idx = torch.from_numpy(idx_np.astype(np.int32)).to(DEV)
+    w = torch.from_numpy(w_np.astype(np.float32)).to(DEV)
+    out = torch.empty((n, hidden), dtype=torch.bfloat16, device=DEV)
+    if fused:
+        idx_out, w_out = torch.empty_like(idx), torch.empty_like(w)
+        heap.pipeline(torch.from_numpy(lg).to(DEV), x, wg, wu, wd, idx_out, w_out, out, fused=1)
+        torch.cuda.synchronize()
+        assert torch.equal(idx_out, idx)
+        w_np = w_out.cpu().numpy()   # the combine's weights, for the oracle's combine
+    else:
+        heap.dispatch(x, idx, w)
+        heap.expert_ffn(wg, wu, wd)
+        heap.combine(idx, w, out)
+    torch.cuda.synchronize()
+    assert heap.status() == 0
+    base = fresh_weight_fn(cfg, DEV)
+
+    def scaled(e):
+        g, u, dn = base(e)
+        sc = lambda b: oracle.round_f64_to_bf16_bits(oracle.bf16_bits_to_f64(b) * scale)
+        return sc(g), sc(u), dn
+    ref = _oracle_from_idx(cfg, idx_np, w_np, scaled)
+    for d in range(cfg["world"]):
+        t = int(ref["tot"][d])
+        assert np.array_equal(bits(heap.recv_x(d)[:t]), ref["rx"][d])
+        assert_close(bits(heap.y(d)[:t]), ref["y_exact"][d], f"H={hidden} I={inter} slot {d} y")
+    assert_close(bits(out), bf16_f64(ref["out"]), f"H={hidden} I={inter} out")
