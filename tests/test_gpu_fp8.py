@@ -130,3 +130,30 @@ def test_fp8_dispatch_full_size_sampled(sm, name):
             d = int(idx_h[g, j]) // (E // W)
             p = int(pos[g, j])
             assert np.array_equal(bits(heap.recv_x(d)[p]), deq[i]), (g, j)
+
+
+def test_fp8_and_dedup_with_weights_in_ffn(sm):
+    """The dispatch variants combine with the weights-in-epilogue variant in
+    the staged pipeline: deduplicated gives the plain dispatch's output bit
+    for bit; FP8 matches the oracle's weights-in-epilogue path on the
+    dequantized rows."""
+    cfg = SMALL["many"]
+    n, k, H = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"], cfg["hidden"]
+    logits = ms.logits_torch(cfg, DEV)
+    x = ms.x_torch(cfg, DEV)
+    wg, wu, wd = ms.weights_torch(cfg, DEV)
+    outs = {}
+    for name, kw in [("plain", {}), ("dedup", {"dedup": True}), ("fp8", {"fp8": True})]:
+        heap = sm.SymHeap(cfg, DEV)
+        idx = torch.empty((n, k), dtype=torch.int32, device=DEV)
+        w = torch.empty((n, k), dtype=torch.float32, device=DEV)
+        out = torch.empty((n, H), dtype=torch.bfloat16, device=DEV)
+        heap.pipeline(logits, x, wg, wu, wd, idx, w, out, weights_in_ffn=True, **kw)
+        torch.cuda.synchronize()
+        assert heap.status() == 0
+        outs[name] = out
+    assert torch.equal(outs["plain"], outs["dedup"])
+    codes, exps = oracle.quantize_rows_e4m3(ms.x_np(cfg))
+    ref = oracle.pipeline(ms.logits_np(cfg), oracle.dequantize_rows(codes, exps), cfg,
+                          fresh_weight_fn(cfg, DEV), weights_in_ffn=True)
+    assert_close(bits(outs["fp8"]), bf16_f64(ref["out"]), "fp8 + weights in the epilogue")
