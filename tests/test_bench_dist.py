@@ -57,3 +57,18 @@ def test_reference_arm_rank_handling(monkeypatch):
     line = json.loads(buf.getvalue())
     assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_traffic_record_only_for_its_workload():
+    """The committed DRAM-traffic record is reported only for the workload
+    and shape it was captured on, and only while its sources are unchanged."""
+    import json
+    import moe_synth as ms
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    name = rec["workload"]
+    cfg = dict(ms.CONFIGS[name])
+    expect = rec["traffic_bytes_per_step"] if rec["sources_sha256"] == bench.sources_sha256() else None
+    assert bench.traffic_record(name, cfg) == expect
+    other = next(k for k in ms.CONFIGS if k != name)
+    assert bench.traffic_record(other, dict(ms.CONFIGS[other])) is None
+    assert bench.traffic_record(name, dict(cfg, tokens_per_slot=cfg["tokens_per_slot"] // 2)) is None
