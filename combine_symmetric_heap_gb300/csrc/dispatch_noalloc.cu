@@ -15,7 +15,9 @@
 // device shares it and it keeps the last call's contents; nothing in it needs
 // to start at zero (the count kernel writes every histogram entry that the
 // scan and the position pass later read).  Calls that overlap on the GPU
-// (different streams without ordering) race on it.
+// (different streams without ordering) race on it.  Its address is looked up
+// on the first call on a device (and again after that device's context was
+// reset), which therefore must not run under stream capture.
 #include <mutex>
 
 #include "symmoe_dev.cuh"
@@ -37,10 +39,14 @@ __global__ void __launch_bounds__(NA_CHUNK)
   __syncthreads();
   const uint32_t bit = 1u << (t & 31);
   const int word = t >> 5;
+  // a token that lists an expert twice sets its bit once: the later copies
+  // (dup, one bit per j) are not placed and get pos -1, so every placed pair
+  // has its own row and the counts add up to the placed pairs
+  uint32_t dup = 0;
   if (g < n) {
     for (int j = 0; j < k; ++j) {
       const int e = idx[(size_t)g * k + j];
-      if (e >= 0 && e < E) atomicOr(&mask[e * (NA_CHUNK / 32) + word], bit);
+      if (e >= 0 && e < E && (atomicOr(&mask[e * (NA_CHUNK / 32) + word], bit) & bit)) dup |= 1u << j;
     }
   }
   __syncthreads();
@@ -48,7 +54,7 @@ __global__ void __launch_bounds__(NA_CHUNK)
     for (int j = 0; j < k; ++j) {
       const int e = idx[(size_t)g * k + j];
       int r = -1;
-      if (e >= 0 && e < E) {
+      if (e >= 0 && e < E && !((dup >> j) & 1u)) {
         const uint32_t *m = mask + e * (NA_CHUNK / 32);
         r = __popc(m[word] & (bit - 1u));
         for (int w = 0; w < word; ++w) r += __popc(m[w]);
@@ -122,24 +128,48 @@ __global__ void __launch_bounds__(256)
 namespace {
 std::mutex g_setup_mu;
 int32_t *g_hist_ptr[64] = {nullptr};
+void *g_hist_ctx[64] = {nullptr};  // the context each address was taken in
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  }
+  return fn;
+}
 }  // namespace
 
-// Device address of the scratch array on the current device (looked up once
-// per device, with that device current).
-static cudaError_t noalloc_scratch(int32_t **out) {
+// Device address of the scratch array on the current device.  Looked up once
+// per device with that device current, and again only if the device's
+// context has changed since (cudaDeviceReset tears the old one down and the
+// array may then sit elsewhere).  A look-up cannot run while `st` is being
+// captured: that case returns SYM_EINVAL.
+static int noalloc_scratch(int32_t **out, cudaStream_t st) {
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SYM_ECUDA;
+  if (dev < 0 || dev >= 64) return SYM_ECUDA;
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_hist_ptr[dev]) {
+  CUcontext ctx = nullptr;
+  CtxGetCurrentFn getctx = ctx_get_current();
+  if (getctx && getctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+  if (!g_hist_ptr[dev] || (ctx && ctx != g_hist_ctx[dev])) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return SYM_ECUDA;
+    if (cap != cudaStreamCaptureStatusNone) return SYM_EINVAL;
     void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_hist);
-    if (e != cudaSuccess) return e;
+    if (cudaGetSymbolAddress(&p, g_noalloc_hist) != cudaSuccess) return SYM_ECUDA;
     g_hist_ptr[dev] = static_cast<int32_t *>(p);
+    g_hist_ctx[dev] = ctx;
   }
   *out = g_hist_ptr[dev];
-  return cudaSuccess;
+  return SYM_OK;
 }
 
 }  // namespace symmoe
@@ -156,16 +186,24 @@ extern "C" int moe_dispatch_layout_noalloc(const moe_shape *s, const int32_t *id
   if (n * k >= (int64_t(1) << 31)) return SYM_EINVAL;
   const int64_t nchunks = (n + NA_CHUNK - 1) / NA_CHUNK;
   if (E * nchunks > SYM_NOALLOC_HIST_MAX) return SYM_ENOSPACE;
-  int32_t *hist = nullptr;
-  if (noalloc_scratch(&hist) != cudaSuccess) return SYM_ECUDA;
   const cudaStream_t st = (cudaStream_t)stream;
+  int32_t *hist = nullptr;
+  const int rc = noalloc_scratch(&hist, st);
+  if (rc != SYM_OK) return rc;
+  // cudaLaunchKernel reports each launch's own error: an error that an
+  // earlier, unrelated launch left behind is neither blamed on this call nor
+  // cleared by it
+  int ni = (int)n, Ei = (int)E, ki = (int)k, Wi = (int)W, nc = (int)nchunks;
   const size_t mask_bytes = (size_t)E * (NA_CHUNK / 32) * sizeof(uint32_t);
-  noalloc_count_kernel<<<(unsigned)nchunks, NA_CHUNK, mask_bytes, st>>>(
-      idx, pos, hist, (int)n, (int)E, (int)k, (int)nchunks);
-  noalloc_scan_kernel<<<1, 1024, 0, st>>>(hist, cnt, recv_off, total_recv, (int)E, (int)W,
-                                          (int)nchunks);
-  noalloc_pos_kernel<<<(unsigned)((n * k + 255) / 256), 256, 0, st>>>(idx, hist, recv_off, pos,
-                                                                       (int)n, (int)E, (int)k,
-                                                                       (int)nchunks);
-  return cudaGetLastError() == cudaSuccess ? SYM_OK : SYM_ECUDA;
+  void *a_count[] = {(void *)&idx, (void *)&pos, (void *)&hist, &ni, &Ei, &ki, &nc};
+  if (cudaLaunchKernel(noalloc_count_kernel, dim3((unsigned)nchunks), dim3(NA_CHUNK), a_count, mask_bytes, st) !=
+      cudaSuccess)
+    return SYM_ECUDA;
+  void *a_scan[] = {(void *)&hist, (void *)&cnt, (void *)&recv_off, (void *)&total_recv, &Ei, &Wi, &nc};
+  if (cudaLaunchKernel(noalloc_scan_kernel, dim3(1), dim3(1024), a_scan, 0, st) != cudaSuccess) return SYM_ECUDA;
+  void *a_pos[] = {(void *)&idx, (void *)&hist, (void *)&recv_off, (void *)&pos, &ni, &Ei, &ki, &nc};
+  if (cudaLaunchKernel(noalloc_pos_kernel, dim3((unsigned)((n * k + 255) / 256)), dim3(256), a_pos, 0, st) !=
+      cudaSuccess)
+    return SYM_ECUDA;
+  return SYM_OK;
 }

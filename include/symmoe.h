@@ -387,7 +387,9 @@ int sym_a2a_gemm(const sym_heap *h, const uint16_t *z, const uint16_t *w, int mo
  * heap's signal area and pos windows:
  *   idx:        device [N][k] int32, N = world * tokens_per_slot; every index
  *               in [0, E) and the k of a token distinct (an index outside
- *               [0, E) is not counted and gets pos -1);
+ *               [0, E) is not counted and gets pos -1; so does every later
+ *               copy of an expert that a token lists twice, which is counted
+ *               once);
  *   cnt:        device [E] int32 (out): pairs per expert;
  *   recv_off:   device [E] int32 (out): first receive row of each expert in
  *               its slot;
@@ -400,8 +402,11 @@ int sym_a2a_gemm(const sym_heap *h, const uint16_t *z, const uint16_t *w, int mo
  * E * ceil(N/128) chunk histograms; larger shapes return SYM_ENOSPACE.  The
  * call makes no device allocation.  Its first call on a device looks up the
  * array's address (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture.  All calls share the array: calls
- * that overlap on the GPU race on it and give wrong results.
+ * first call before any stream capture.  The address is kept per device and
+ * looked up again on the first call after the device's context changed (after
+ * cudaDeviceReset): that call, too, must come before any capture (under
+ * capture it returns SYM_EINVAL).  All calls share the array: calls that
+ * overlap on the GPU race on it and give wrong results.
  * Asynchronous on `stream`; SYM_OK, SYM_EINVAL, SYM_ENOSPACE or SYM_ECUDA.
  */
 #define SYM_NOALLOC_HIST_MAX (1 << 18)

@@ -1,0 +1,61 @@
+"""Host logic of the benchmark on CPU: the per-expert roof, the per-workload
+record's entries, and the one-core leg of the oracle timing (BLAS threads and
+the calling thread's affinity are restored afterwards)."""
+import os
+
+import numpy as np
+
+import bench
+
+CFG = dict(world=8, tokens_per_slot=1024, hidden=7168, num_experts=256, topk=8, inter=2048)
+
+
+def test_per_expert_roof_single_expert_is_its_own_roof():
+    H, I = CFG["hidden"], CFG["inter"]
+    for c in (1, 256, 100000):
+        counts = np.zeros(256, dtype=np.int64)
+        counts[3] = c
+        flops = 6.0 * c * H * I
+        bts = 3.0 * H * I * 2 + 4.0 * c * H + 4.0 * c * I
+        want = max(flops / 2e15, bts / 8e12)
+        assert np.isclose(bench.per_expert_roof_s(CFG, counts, 2000.0, 8000.0), want, rtol=1e-12)
+
+
+def test_per_expert_roof_bounds():
+    """The sum of per-expert roofs is never below the plain roof (max of the
+    sums) and never above the sum of both times; empty experts cost nothing."""
+    rng = np.random.default_rng(1)
+    H, I = CFG["hidden"], CFG["inter"]
+    for _ in range(5):
+        counts = rng.zipf(1.5, size=256).clip(max=8192) * (rng.random(256) < 0.7)
+        t = bench.per_expert_roof_s(CFG, counts, 1900.0, 6700.0)
+        flops = sum(6.0 * c * H * I for c in counts)
+        bts = sum(3.0 * H * I * 2 + 4.0 * c * H + 4.0 * c * I for c in counts if c > 0)
+        tf, tb = flops / 1.9e15, bts / 6.7e12
+        assert max(tf, tb) * (1 - 1e-12) <= t <= (tf + tb) * (1 + 1e-12)
+    assert bench.per_expert_roof_s(CFG, np.zeros(256, dtype=np.int64), 1900.0, 6700.0) == 0.0
+
+
+def test_workload_summary_entry():
+    counts = np.full(256, 256, dtype=np.int64)
+    stages = {"route": 0.01, "dispatch": 0.2, "expert_ffn": 4.5, "combine": 0.17}
+    e = bench.workload_summary("deepseek", CFG, 0, 20, 20 * 4.9, stages, None, counts)
+    assert e["fused"] is False and e["ms_per_step"] == 4.9
+    assert np.isclose(e["tokens_per_s"], 8192 / 4.9e-3)
+    assert e["ffn_roof"]["bound"] in ("hbm", "tensor") and 0 < e["ffn_roof"]["frac"] < 2
+    assert e["stage_bandwidth"]["dispatch_frac"] > 0 and e["experts_hit"] == 256
+    f = bench.workload_summary("decode", CFG, 1, 20, 20 * 3.5, {"fused": 3.5}, None, counts)
+    assert "dispatch_frac" not in f["stage_bandwidth"] and f["fused"] is True
+
+
+def test_one_core_leg_restores_threads_and_affinity():
+    before_threads = bench.blas_threads()
+    before_aff = os.sched_getaffinity(0)
+    with bench.OneCore() as one:
+        if one.getf is not None:
+            assert one.threads == 1
+        assert len(os.sched_getaffinity(0)) == 1
+        a = np.ones((64, 64))
+        assert (a @ a)[0, 0] == 64.0
+    assert bench.blas_threads() == before_threads
+    assert os.sched_getaffinity(0) == before_aff
