@@ -36,6 +36,8 @@ SYM_STATUS_TIMEOUT = 0x1
 SYM_STATUS_OVERFLOW = 0x2
 SYM_ROWS_PER_FLAG = 128
 SYM_COUNT_CHUNK = 128
+SYM_GUARD_BYTES = 1024
+SYM_HEAP_WINDOWS = 13
 
 _u64 = ctypes.c_uint64
 _u32 = ctypes.c_uint32
@@ -80,6 +82,7 @@ def lib() -> ctypes.CDLL:
         L.sym_heap_init.argtypes = [P(MoeShape), _vp, _u64, _u64, P(SymHeapDesc)]
         L.sym_heap_slot_ptr.argtypes = [P(SymHeapDesc), ctypes.c_int, _u64]
         L.sym_heap_slot_ptr.restype = _vp
+        L.sym_heap_windows.argtypes = [P(SymHeapDesc), P(_u64), P(_u64), ctypes.c_int]
         L.moe_route_topk.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
         L.moe_router_logits.argtypes = [P(SymHeapDesc), _vp, _vp, _vp, _vp]
         L.moe_router_splits.argtypes = [P(SymHeapDesc), P(ctypes.c_int)]
@@ -255,6 +258,16 @@ def moe_dispatch_layout_noalloc(shape, idx, cnt, recv_off, total_recv, pos, stre
            "moe_dispatch_layout_noalloc")
 
 
+def sym_heap_windows(heap: SymHeapDesc) -> list:
+    """(offset, bytes) of every window inside a slot, in layout order."""
+    n = SYM_HEAP_WINDOWS
+    offs, sizes = (_u64 * n)(), (_u64 * n)()
+    rc = lib().sym_heap_windows(ctypes.byref(heap), offs, sizes, n)
+    if rc < 0:
+        raise SymmoeError(rc, "sym_heap_windows")
+    return [(int(offs[i]), int(sizes[i])) for i in range(rc)]
+
+
 def sym_heap_status(heap: SymHeapDesc, clear: bool = False, stream=None) -> int:
     st = _i32()
     _check(lib().sym_heap_status(ctypes.byref(heap), ctypes.byref(st), int(clear), _stream(stream)),
@@ -335,6 +348,15 @@ class SymHeap:
 
     def status(self, clear: bool = False, stream=None) -> int:
         return sym_heap_status(self.desc, clear, stream)
+
+    def guard_bands(self) -> list:
+        """(start, length) byte ranges of ``self.buf`` that no call touches:
+        the bands after every window of every slot."""
+        wins = sym_heap_windows(self.desc)
+        prs = self.desc.per_rank_size
+        ends = [o + b for o, b in wins]
+        starts = [o for o, _ in wins[1:]] + [prs]
+        return [(d * prs + e, s - e) for d in range(self.shape["world"]) for e, s in zip(ends, starts)]
 
     # calls -----------------------------------------------------------------
     def route_topk(self, logits, idx, w, stream=None):

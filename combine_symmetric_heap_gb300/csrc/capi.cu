@@ -4,9 +4,10 @@
 // Heap layout (MORI CCO guide, "3. Memory and Windows": windows are registered
 // collectively, in the same order and with the same size on every rank, so
 // each sits at the same offset in every slot).  Windows of one slot, in this
-// order, each 1024-byte aligned: recv_x, y, h, recv_pair, recv_w, pos, cnt,
-// recv_off, total, status, ready, hist, ctrl.  per_rank_size is the sum rounded
-// up to the caller's alignment.
+// order, each 1024-byte aligned and followed by a guard band of at least
+// SYM_GUARD_BYTES: recv_x, y, h, recv_pair, recv_w, pos, cnt, recv_off, total,
+// status, ready, hist, ctrl.  per_rank_size is the sum rounded up to the
+// caller's alignment.
 #include <atomic>
 #include <cstring>
 
@@ -67,6 +68,7 @@ struct Layout {
   uint64_t cap, off_recv_x, off_y, off_h, off_recv_pair, off_recv_w, off_pos, off_cnt,
       off_recv_off, off_total, off_status, off_ready, off_hist, off_ctrl, used;
   uint32_t num_ready;
+  uint64_t win_off[SYM_HEAP_WINDOWS], win_bytes[SYM_HEAP_WINDOWS];  // in slot order
 };
 
 Layout layout_of(const moe_shape *s) {
@@ -77,9 +79,14 @@ Layout layout_of(const moe_shape *s) {
   L.cap = N * (k < E_loc ? k : E_loc);
   L.num_ready = (uint32_t)((L.cap + SYM_ROWS_PER_FLAG - 1) / SYM_ROWS_PER_FLAG);
   uint64_t o = 0;
+  int nwin = 0;
+  // every window is followed by at least SYM_GUARD_BYTES that no call reads
+  // or writes (a guard band: a store past a window's end lands there first)
   auto take = [&](uint64_t bytes) {
     const uint64_t at = o;
-    o = round_up(o + bytes, kWinAlign);
+    L.win_off[nwin] = at;
+    L.win_bytes[nwin++] = bytes;
+    o = round_up(o + bytes + SYM_GUARD_BYTES, kWinAlign);
     return at;
   };
   L.off_recv_x = take(L.cap * H * 2);
@@ -173,6 +180,16 @@ int sym_heap_init(const moe_shape *s, void *dev_base, uint64_t bytes, uint64_t a
   h.s = *s;
   *out = h;
   return SYM_OK;
+}
+
+int sym_heap_windows(const sym_heap *h, uint64_t *offsets, uint64_t *bytes, int max_windows) {
+  if (!heap_ok(h) || max_windows < 0 || (max_windows > 0 && (!offsets || !bytes))) return SYM_EINVAL;
+  const Layout L = layout_of(&h->s);
+  for (int i = 0; i < SYM_HEAP_WINDOWS && i < max_windows; ++i) {
+    offsets[i] = L.win_off[i];
+    bytes[i] = L.win_bytes[i];
+  }
+  return SYM_HEAP_WINDOWS;
 }
 
 void *sym_heap_slot_ptr(const sym_heap *h, int slot, uint64_t offset) {

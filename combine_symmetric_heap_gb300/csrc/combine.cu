@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(256)
     stage_expert_out_kernel(sym_heap h, const uint4 *__restrict__ expert_out) {
   const int d = blockIdx.y;
   const int nvec = h.s.hidden / 8;
-  const int total = *win<const int32_t>(h, d, h.off_total);
+  const int total = checked_total(h, d, blockIdx.x == 0 && threadIdx.x == 0);
   const uint4 *src = expert_out + (size_t)d * h.cap * nvec;
   uint4 *dst = win<uint4>(h, d, h.off_y);
   const size_t n = (size_t)total * nvec;

@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(SCATTER_THREADS) dedup_expand_kernel(sym_heap 
   const int tid = threadIdx.x;
   pdl_launch_dependents();
   pdl_wait();  // the staged rows and the row sources
-  const int total = *win<const int32_t>(h, d, h.off_total);
+  const int total = checked_total(h, d, blockIdx.x == 0 && tid == 0);
   for (int p = (int)blockIdx.x; p < total; p += (int)gridDim.x) {
     const int q = win<const int32_t>(h, d, h.off_h)[p];
     if (q < 0 || q >= N) {
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(SCATTER_THREADS) fp8_dequant_kernel(sym_heap h
   const int tid = threadIdx.x;
   pdl_launch_dependents();
   pdl_wait();  // the codes and the scales
-  const int total = *win<const int32_t>(h, d, h.off_total);
+  const int total = checked_total(h, d, blockIdx.x == 0 && tid == 0);
   for (int p = (int)blockIdx.x; p < total; p += (int)gridDim.x) {
     const float sc = win<const float>(h, d, h.off_h)[p];
     const uint2 *src = reinterpret_cast<const uint2 *>(win<const uint8_t>(h, d, h.off_y) + (size_t)p * H);

@@ -412,7 +412,9 @@ __device__ inline void combine_token(const sym_heap &h, const FusedArgs &a, cons
     const int e = __ldcg(a.idx + (size_t)g * k + lane);
     const int p = __ldcg(win<const int32_t>(h, g / T, h.off_pos) + (size_t)(g % T) * k + lane);
     const uint4 *src = nullptr;
-    if (p >= 0) {
+    if (p >= 0 && (p < tb.roff[e] || p >= tb.roff[e] + tb.cnt[e])) {
+      raise_status(h, SYM_STATUS_OVERFLOW);  // a row outside its expert's tiles: skipped
+    } else if (p >= 0) {
       // the 256-row down tile holding this row: every epilogue warp of every
       // feature tile has stored its share
       ok = wait_geq(h, y_ready(h) + tb.tokprefix[e] + gemm2::tile_of_row(tb.cnt[e], p - tb.roff[e]),
@@ -493,7 +495,9 @@ __device__ inline void combine_token_stream(const sym_heap &h, const FusedArgs &
     const int e = __ldcg(a.idx + (size_t)g * k + lane);
     const int p = __ldcg(win<const int32_t>(h, g / T, h.off_pos) + (size_t)(g % T) * k + lane);
     const uint4 *src = nullptr;
-    if (p >= 0) {
+    if (p >= 0 && (p < tb.roff[e] || p >= tb.roff[e] + tb.cnt[e])) {
+      raise_status(h, SYM_STATUS_OVERFLOW);  // a row outside its expert's tiles: skipped
+    } else if (p >= 0) {
       ok = wait_geq(h, y_ready(h) + tb.tokprefix[e] + gemm2::tile_of_row(tb.cnt[e], p - tb.roff[e]), target);
       src = win<const uint4>(h, e / E_loc, h.off_y) + (size_t)p * (H / 8);
     }

@@ -126,13 +126,23 @@ __host__ __device__ constexpr size_t tok_tables_bytes(int num_experts) {
   return (size_t)(3 * num_experts + 1) * sizeof(int);
 }
 // Reads the dispatch results with __ldcg: in the fused pipeline they were
-// written earlier in the same launch.
+// written earlier in the same launch.  An expert whose rows [off, off + cnt)
+// do not lie inside its slot's windows (a corrupted or stale signal area)
+// gets no tiles: the tables say it has no rows, so no tile reads or stores
+// past the capacity, and SYM_STATUS_OVERFLOW is raised.
 __device__ inline void build_tok_tables(const sym_heap &h, const TokTables &tb) {
   const int E = h.s.num_experts, E_loc = E / h.s.world;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int d = e / E_loc, l = e % E_loc;
-    tb.cnt[e] = __ldcg(win<const int32_t>(h, d, h.off_cnt) + l);
-    tb.roff[e] = __ldcg(win<const int32_t>(h, d, h.off_recv_off) + l);
+    int c = __ldcg(win<const int32_t>(h, d, h.off_cnt) + l);
+    int o = __ldcg(win<const int32_t>(h, d, h.off_recv_off) + l);
+    if (c < 0 || o < 0 || (uint64_t)o + (uint64_t)c > h.cap) {
+      raise_status(h, SYM_STATUS_OVERFLOW);
+      c = 0;
+      o = 0;
+    }
+    tb.cnt[e] = c;
+    tb.roff[e] = o;
   }
   __syncthreads();
   if (threadIdx.x < 32) {
@@ -692,7 +702,7 @@ __device__ bool epi_tile(const sym_heap &h, const Pipe &p, EpiState &s, const Ti
 template <typename Wait>
 __device__ bool rows_ready(const sym_heap &h, int d, int row, int n, bool block, Wait wait) {
   if (n <= 0) return true;
-  const int total = __ldcg(win<const int32_t>(h, d, h.off_total));
+  const int total = checked_total(h, d, true);
   const uint32_t *ready = win<const uint32_t>(h, d, h.off_ready);
   for (int b = row / SYM_ROWS_PER_FLAG; b <= (row + n - 1) / SYM_ROWS_PER_FLAG; ++b) {
     const uint32_t target = (uint32_t)min(SYM_ROWS_PER_FLAG, total - b * SYM_ROWS_PER_FLAG);

@@ -29,6 +29,18 @@ __device__ __forceinline__ int32_t *status_word(const sym_heap &h) {
 __device__ __forceinline__ void raise_status(const sym_heap &h, int bits) {
   atomicOr(status_word(h), bits);
 }
+// Rows slot d received in the last dispatch, checked against the window
+// capacity before any kernel sizes its loops by it: a total outside
+// [0, cap] (a corrupted or stale signal area) is reported as
+// SYM_STATUS_OVERFLOW (when `report`) and taken as 0, so no row is touched.
+__device__ __forceinline__ int checked_total(const sym_heap &h, int d, bool report) {
+  const int t = __ldcg(reinterpret_cast<const int32_t *>(slot_ptr(h, d, h.off_total)));
+  if (t < 0 || (uint64_t)t > h.cap) {
+    if (report) raise_status(h, SYM_STATUS_OVERFLOW);
+    return 0;
+  }
+  return t;
+}
 
 // ---------------------------------------------------------------------------
 // bf16 helpers (round-to-nearest-even through the CUDA intrinsics)

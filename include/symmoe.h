@@ -102,9 +102,19 @@ typedef struct moe_shape {
  *                ready [ceil(cap/128)] uint32 (rows landed per 128-row block)
  *   scratch (used in slot 0 only): dispatch chunk histograms, fused-kernel
  *                control block.
+ * Every window is followed by a guard band of at least SYM_GUARD_BYTES that
+ * no call reads or writes (sym_heap_windows gives each window's extent), so
+ * a caller or a test can fill the bands with a pattern and check it after a
+ * call.  Counts the kernels read back from the signal area are checked
+ * against the window capacity: an expert whose rows [recv_off, recv_off +
+ * cnt) or a slot whose total_recv do not fit in [0, cap) is skipped and
+ * SYM_STATUS_OVERFLOW is raised (a corrupted or stale signal area never
+ * sends a store past a window).
  * Receive rows are grouped by expert (ascending) inside a slot; inside one
  * expert they are in (source slot, token, k) order.
  */
+#define SYM_GUARD_BYTES 1024
+#define SYM_HEAP_WINDOWS 13
 typedef struct sym_heap {
   uint64_t base;          /* device address of slot 0                          */
   uint64_t per_rank_size; /* slot stride in bytes (multiple of align)          */
@@ -153,6 +163,18 @@ int sym_heap_init(const moe_shape *s, void *dev_base, uint64_t bytes, uint64_t a
  * of "What is MORI CCO?").  Returns NULL if slot or offset is out of range.
  */
 void *sym_heap_slot_ptr(const sym_heap *h, int slot, uint64_t offset);
+
+/*
+ * sym_heap_windows: the extent of every window inside a slot, in layout
+ * order (recv_x, y, h, recv_pair, recv_w, pos, cnt, recv_off, total_recv,
+ * status, ready, hist, ctrl): offsets[i] and bytes[i] for the first
+ * min(max_windows, SYM_HEAP_WINDOWS) windows.  The bytes between the end of
+ * window i and the start of window i + 1 (and after the last window, up to
+ * per_rank_size) are the guard bands, at least SYM_GUARD_BYTES each.  Not in
+ * the pages: a checking aid (a layout with guard bands stands in for a
+ * memory checker).  Host only.  Returns SYM_HEAP_WINDOWS, or SYM_EINVAL.
+ */
+int sym_heap_windows(const sym_heap *h, uint64_t *offsets, uint64_t *bytes, int max_windows);
 
 /*
  * moe_route_topk: per token, the top-k of E fp32 logits (descending, ties to

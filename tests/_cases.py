@@ -81,18 +81,45 @@ def fresh_weight_fn(cfg: dict, device, seed: int = 0):
     return fn
 
 
+# Canaries: a byte pattern planted in the heap's guard bands (the bytes after
+# every window that no call may touch) and checked after each call.  A kernel
+# that stores past the end of a window (a row beyond capacity, a count it
+# trusted) changes a band before anything else.
+CANARY = 0xA5
+
+
+def plant_canaries(heap) -> None:
+    for start, length in heap.guard_bands():
+        heap.buf[start:start + length].fill_(CANARY)
+
+
+def assert_canaries(heap, what: str) -> None:
+    torch.cuda.synchronize()
+    bad = [(s, n) for s, n in heap.guard_bands() if not bool((heap.buf[s:s + n] == CANARY).all())]
+    assert not bad, f"{what}: guard bands changed at {bad[:4]} (of {len(heap.guard_bands())})"
+
+
 def run_gpu_stages(sm, cfg: dict, logits, x, wg, wu, wd, heap=None, idx=None, w=None):
-    """route -> dispatch -> expert FFN -> combine, one call per stage."""
+    """route -> dispatch -> expert FFN -> combine, one call per stage.  On a
+    heap it creates, canaries are planted first and checked after every call."""
     dev = x.device
     n, k = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"]
+    fresh = heap is None
     heap = heap or sm.SymHeap(cfg, dev)
+    check = (lambda what: assert_canaries(heap, what)) if fresh else (lambda what: None)
+    if fresh:
+        plant_canaries(heap)
     if idx is None:
         idx = torch.empty((n, k), dtype=torch.int32, device=dev)
         w = torch.empty((n, k), dtype=torch.float32, device=dev)
         heap.route_topk(logits, idx, w)
+        check("route")
     heap.dispatch(x, idx, w)
+    check("dispatch")
     heap.expert_ffn(wg, wu, wd)
+    check("expert FFN")
     out = torch.empty((n, cfg["hidden"]), dtype=torch.bfloat16, device=dev)
     heap.combine(idx, w, out)
+    check("combine")
     torch.cuda.synchronize()
     return heap, idx, w, out

@@ -72,8 +72,10 @@ def test_heap_layout(name):
             # tile + a route-task counter per 32-token chunk
             (d.off_ctrl, 4 * (64 + 2 * (n * k // 256 + cfg["num_experts"] + 1) + (n + 31) // 32))]
     for (o, b), (o2, _) in zip(wins, wins[1:]):
-        assert o % 1024 == 0 and o + b <= o2
-    assert wins[-1][0] + wins[-1][1] <= prs
+        assert o % 1024 == 0 and o + b + sm.SYM_GUARD_BYTES <= o2   # a guard band after every window
+    assert wins[-1][0] + wins[-1][1] + sm.SYM_GUARD_BYTES <= prs
+    # the library's own account of the windows is the same layout
+    assert sm.sym_heap_windows(d) == [(int(o), int(b)) for o, b in wins]
     assert d.num_ready == (d.cap + 127) // 128
     assert d.wait_timeout_us == 2_000_000 and d.epoch == 0
 
