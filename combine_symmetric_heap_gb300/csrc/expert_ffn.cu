@@ -19,8 +19,10 @@
 //            the tcgen05.mma; two accumulator buffers let the epilogue of
 //            tile i overlap the main loop of tile i+1;
 //   warps 2-5 epilogue: tcgen05.ld, SwiGLU / bf16 rounding, stores.
-// Pair tiles follow a rotated static schedule (pair_tile); row counts come from the dispatch signal
-// area on the device (no host sync).
+// Pairs claim tiles dynamically (the leader's producer takes the next index
+// from a counter in the heap's control window and hands it to the pair's
+// other roles, gemm2sm.cuh); row counts come from the dispatch signal area on
+// the device (no host sync).
 #include <mutex>
 
 #include "gemm2sm.cuh"
@@ -33,6 +35,10 @@ constexpr int GEMM_THREADS = 192;
 // CTA-pair (cta_group::2) expert GEMM, used by moe_expert_ffn
 // ---------------------------------------------------------------------------
 constexpr int G2_CTRL_BYTES = 256;
+// words of slot 0's control window used by the staged expert GEMM's dynamic
+// schedule: per kind the next tile to claim and the CTAs done (the last CTA
+// out resets both, so every launch starts from zero)
+constexpr int G2_SCHED_WORD = 32;
 
 static size_t gemm2_smem_bytes(int num_experts) {
   return 1024 + (size_t)gemm2::STAGES * gemm2::STAGE_BYTES + gemm2::XCH_BYTES + G2_CTRL_BYTES +
@@ -50,14 +56,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *ctrl = smem + (size_t)STAGES * STAGE_BYTES + XCH_BYTES;
   uint64_t *bars = reinterpret_cast<uint64_t *>(ctrl);  // full[6] empty[6] acc_full[2] acc_empty[2] acc_head[2]
-  uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 6);
+  // tile queue: full[TQ] empty[TQ] after the ring barriers, then the words
+  const TileQueue tq{reinterpret_cast<volatile int *>(bars + 2 * STAGES + 6 + 2 * TQ + 2),
+                     bars + 2 * STAGES + 6, bars + 2 * STAGES + 6 + TQ};
+  uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 6 + 2 * TQ);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base_s + 1);
   volatile int *stop_tile = abort_flag + 1;
   const int E = h.s.num_experts;
   int *tab = reinterpret_cast<int *>(ctrl + G2_CTRL_BYTES);
   const TokTables tb{tab, tab + E, tab + 2 * E};
   const int wid = warp_id(), lane = lane_id();
-  const int pair_id = (int)cluster_id_x(), npairs = (int)num_clusters_x();
   Pipe p;
   p.ring = smem;
   p.xch = reinterpret_cast<float *>(smem + (size_t)STAGES * STAGE_BYTES);
@@ -82,6 +90,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(&p.acc_empty[b], 8);  // leader: 4 epilogue warps of each CTA
       mbar_init(&p.acc_head[b], 8);
     }
+    tq_init(tq);
     *abort_flag = 0;
     *stop_tile = 0x7fffffff;
     fence_mbar_init();
@@ -103,56 +112,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   const int total_tiles = tb.tokprefix[E] * nf;
   const uint32_t tmo = h.wait_timeout_us;
   auto wait = [&](const uint32_t *c, uint32_t target) { return wait_counter_geq(c, target, tmo, abort_flag); };
-  // the token rows of tile t dispatched (both CTAs check the whole tile)
-  auto tile_ready = [&](int t, bool block) {
-    const TileInfo ti = decode_tok(h, tb, nf, grp, t);
-    return rows_ready(h, ti.d, ti.row0, ti.valid, block, wait);
-  };
+  uint32_t *sched = win<uint32_t>(h, 0, h.off_ctrl) + G2_SCHED_WORD + 2 * KIND;  // next tile, CTAs done
 
+  // Every role walks the pair's schedule by entry n; the stop bound and the
+  // wait bounds count entries.
   if (wid == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
       ProdState ps;
-      int i = 0, t = pair_tile(0, pair_id, npairs);
-      bool ready_ok = true;
-      if (wait_ready && t < total_tiles) {
-        ready_ok = tile_ready(t, true);
-        if (!ready_ok) {
-          raise_status(h, SYM_STATUS_TIMEOUT);
-          *stop_tile = t;
-        }
-      }
-      while (ready_ok && t < total_tiles && !*abort_flag) {
-        if (wait_ready) fence_proxy_async();  // rows written by generic stores
+      auto claim = [&]() {
+        const int t = (int)atomicAdd(sched, 1u);
+        return t < total_tiles ? t : -1;
+      };
+      // the tile's token rows dispatched (the whole tile, both CTAs' halves)
+      auto ready = [&](int t, bool block) {
+        if (!wait_ready) return true;
         const TileInfo ti = decode_tok(h, tb, nf, grp, t);
-        const int t_next = pair_tile(i + 1, pair_id, npairs);
-        bool next_ok = !wait_ready || t_next >= total_tiles;
-        auto probe = [&]() {
-          if (!next_ok) next_ok = tile_ready(t_next, false);
-        };
-        if (!produce_tile<KIND>(h, p, ps, ti, &tm_a0, &tm_a1, tm_b, t, probe)) break;
-        if (!next_ok && !tile_ready(t_next, true)) {
-          raise_status(h, SYM_STATUS_TIMEOUT);
-          *stop_tile = t_next;
-          break;
-        }
-        t = t_next;
-        ++i;
-      }
+        return rows_ready(h, ti.d, ti.row0, ti.valid, block, wait);
+      };
+      auto produce = [&](int t, int n, auto &probe) {
+        return produce_tile<KIND>(h, p, ps, decode_tok(h, tb, nf, grp, t), &tm_a0, &tm_a1, tm_b, n, probe);
+      };
+      produce_schedule(h, p, tq, stop_tile, claim, ready, produce);
     }
   } else if (wid == 1) {
     if (lane == 0 && p.rank == 0) {
       // ---------------------------------------------------- MMA issuer (leader)
       MmaState ms;
-      for (int i = 0, t; (t = pair_tile(i, pair_id, npairs)) < total_tiles; ++i)
-        if (!mma_tile<KIND>(h, p, ms, decode_tok(h, tb, nf, grp, t), t)) break;
+      for (int n = 0;; ++n) {
+        const int t = tq_pop(h, p, tq, n);
+        if (t < 0 || !mma_tile<KIND>(h, p, ms, decode_tok(h, tb, nf, grp, t), n)) break;
+      }
     }
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = wid & 3;  // TMEM lane quarter this warp may access
     EpiState es;
-    for (int i = 0, t; (t = pair_tile(i, pair_id, npairs)) < total_tiles; ++i)
-      if (!epi_tile<KIND>(h, p, es, decode_tok(h, tb, nf, grp, t), t, q, lane)) break;
+    for (int n = 0;; ++n) {
+      int t = 0;
+      if (lane == 0) t = tq_pop(h, p, tq, n);  // lane 0 reads the entry and hands it back
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (t < 0 || !epi_tile<KIND>(h, p, es, decode_tok(h, tb, nf, grp, t), n, q, lane)) break;
+    }
   }
 
   tc_fence_before();
@@ -160,6 +161,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   cluster_sync();  // no remote arrive or MMA of the pair is still in flight
   tc_fence_after();
   if (wid == 1) tmem_dealloc2(p.tmem_base, TMEM_COLS);
+  if (threadIdx.x == 0) {
+    // every pair has claimed past the end: the last CTA out resets the schedule
+    __threadfence();
+    if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+      sched[0] = 0u;
+      __threadfence();
+      sched[1] = 0u;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------

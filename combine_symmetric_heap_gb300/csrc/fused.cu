@@ -20,8 +20,9 @@
 //            destination slot's recv_x window; each row raises the ready
 //            counter of its 128-row block (release).
 //   phase 3  expert GEMM tiles on CTA pairs (the tcgen05 cta_group::2 tiles of
-//            the stand-alone GEMM): each pair takes its gate/up tiles, then its
-//            down tiles, in the rotated static schedule of the pair engine.  A gate/up tile starts once the ready
+//            the stand-alone GEMM): pairs claim tiles from one counter, every
+//            gate/up tile before any down tile (the pair engine's dynamic
+//            schedule).  A gate/up tile starts once the ready
 //            counters of its token rows are complete; a down tile once every
 //            gate/up feature tile of its 256 token rows is stored (h_ready);
 //            each epilogue warp of both CTAs bumps h_ready / y_ready of the
@@ -30,10 +31,9 @@
 //
 // Forward progress: phases 1, 2 and 4 claim work from per-phase counters and
 // a CTA moves on only after finding the previous phase's counter exhausted, so
-// a task only waits for work already claimed by a running CTA; phase 3's tiles
-// are assigned statically to pairs, which is safe because the grid holds only
-// as many pairs as can be resident at once and a pair finishes its gate/up
-// tiles before its down tiles.  Every wait is also bounded by the heap's
+// a task only waits for work already claimed by a running CTA; in phase 3 a
+// down tile waits only on gate/up tiles, all of which were claimed before it
+// by resident pairs that stream them without waiting on any down tile.  Every wait is also bounded by the heap's
 // wait_timeout_us (on expiry: SYM_STATUS_TIMEOUT, a global abort flag, and
 // every CTA skips the rest of its work).  The last CTA to exit resets the
 // counters, so the next launch on the stream starts clean.
@@ -64,6 +64,7 @@ enum Ctl : int {
   C_EXIT = 7,
   C_ABORT = 8,
   C_SCAN_TASKS = 9,  // per-expert scan tasks completed
+  C_TILE_NEXT = 10,  // GEMM tiles claimed (gate/up tiles first, then down tiles)
   C_WORDS = 64
 };
 
@@ -586,9 +587,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
   uint8_t *ctrl_s = xch_raw + XCH_BYTES;
   uint64_t *bars = reinterpret_cast<uint64_t *>(ctrl_s);  // full[6] empty[6] acc_full[2] acc_empty[2] acc_head[2]
   uint64_t *drained = bars + 2 * STAGES + 6;  // every MMA of this launch has completed
+  // tile queue of the dynamic schedule at ctrl_s + 168 (barriers) and + 232 (entries)
+  const TileQueue tq{reinterpret_cast<volatile int *>(ctrl_s + 232), reinterpret_cast<uint64_t *>(ctrl_s + 168),
+                     reinterpret_cast<uint64_t *>(ctrl_s + 168) + TQ};
   uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(drained + 1);
   volatile int *abort_s = reinterpret_cast<volatile int *>(tmem_base_s + 1);
-  volatile int *never_s = abort_s + 1;  // "stop before tile" bound: never
+  volatile int *never_s = abort_s + 1;  // stop bound of the schedule: the entry where this CTA stopped
   int *bcast = const_cast<int *>(never_s + 1);
   // per-warp row-slot barriers of the scatter phase
   uint64_t *sbar = reinterpret_cast<uint64_t *>(ctrl_s + 256) + warp_id() * SCATTER_SLOTS_MAX;
@@ -602,7 +606,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
   float *wgt_s = reinterpret_cast<float *>(xch_raw + FUSED_THREADS / 32 * 32 * sizeof(void *)) + wid * 32;
   const int N = h.s.world * h.s.tokens_per_slot;
   const int nchunks = (N + FUSED_CHUNK - 1) / FUSED_CHUNK;
-  const int pair_id = (int)cluster_id_x(), npairs = (int)num_clusters_x();
+
   Pipe p;
   p.ring = ring;
   p.xch = reinterpret_cast<float *>(xch_raw);
@@ -628,6 +632,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
       mbar_init(&p.acc_head[b], 8);
     }
     mbar_init(drained, 1);
+    tq_init(tq);
     uint64_t *sbar0 = reinterpret_cast<uint64_t *>(ctrl_s + 256);
     for (int i = 0; i < FUSED_THREADS / 32 * SCATTER_SLOTS_MAX; ++i) mbar_init(&sbar0[i], 1);
     *abort_s = 0;
@@ -765,55 +770,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
       }
       return rows_ready(h, ti.d, ti.row0, ti.valid, block, wait);
     };
-    // the pair's tiles: its gate/up tiles, then its down tiles, each list in
-    // the rotated static schedule; (kind, i) = the pair's i-th tile of a list
-    auto tile_at = [&](int i) { return pair_tile(i, pair_id, npairs); };
-    auto valid_at = [&](int kind, int i) { return tile_at(i) < (kind == GATE_UP ? total1 : total2); };
-    auto next_of = [&](int &kind, int &i) {
-      ++i;
-      if (kind == GATE_UP && !valid_at(GATE_UP, i)) {
-        kind = DOWN;
-        i = 0;
-      }
+    // The pair's tiles, claimed from one counter: claim c < total1 is gate/up
+    // tile c, else down tile c - total1.  Every role walks the schedule by
+    // entry n (gemm2sm.cuh, TileQueue).
+    uint32_t *next = ctl(h) + C_TILE_NEXT;
+    auto kind_of = [&](int c) { return c < total1 ? GATE_UP : DOWN; };
+    auto tile_of = [&](int c) { return c < total1 ? c : c - total1; };
+    auto info_of = [&](int c) {
+      return c < total1 ? decode_tok(h, tb, nf1, g1, c) : decode_tok(h, tb, nf2, g2, c - total1);
     };
-    int kind0 = GATE_UP;
-    if (!valid_at(GATE_UP, 0)) kind0 = DOWN;
-
     if (wid == 0) {
       if (lane == 0) {
         // ------------------------------------------------------------ producer
         ProdState ps;
-        int kind = kind0, i = 0;
-        bool ok = valid_at(kind, i) ? inputs_ready(kind, tile_at(i), true) : true;
-        while (ok && valid_at(kind, i) && !*abort_s) {
-          fence_proxy_async();  // the inputs were written by generic stores in this launch
-          const int t = tile_at(i);
-          int kind_n = kind, i_n = i;
-          next_of(kind_n, i_n);
-          const bool has_next = valid_at(kind_n, i_n);
-          const int t_n = tile_at(i_n);
-          bool next_ok = !has_next;
-          auto probe = [&]() {
-            if (!next_ok) next_ok = inputs_ready(kind_n, t_n, false);
-          };
-          ok = kind == GATE_UP
-                   ? produce_tile<GATE_UP>(h, p, ps, decode_tok(h, tb, nf1, g1, t), &tm_g, &tm_u, tm_rx, -1, probe)
-                   : produce_tile<DOWN>(h, p, ps, decode_tok(h, tb, nf2, g2, t), &tm_d, &tm_d, tm_h, -1, probe);
-          if (!ok) break;
-          if (has_next && !next_ok) ok = inputs_ready(kind_n, t_n, true);
-          kind = kind_n;
-          i = i_n;
-        }
-        if (!ok) *abort_s = 1;
+        auto claim = [&]() {
+          const int c = (int)atomicAdd(next, 1u);
+          return c < total1 + total2 ? c : -1;
+        };
+        auto ready = [&](int c, bool block) { return inputs_ready(kind_of(c), tile_of(c), block); };
+        auto produce = [&](int c, int n, auto &probe) {
+          return kind_of(c) == GATE_UP
+                     ? produce_tile<GATE_UP>(h, p, ps, info_of(c), &tm_g, &tm_u, tm_rx, n, probe)
+                     : produce_tile<DOWN>(h, p, ps, info_of(c), &tm_d, &tm_d, tm_h, n, probe);
+        };
+        if (!produce_schedule(h, p, tq, never_s, claim, ready, produce)) *abort_s = 1;
       }
     } else if (wid == 1) {
       if (lane == 0 && p.rank == 0) {
         // ------------------------------------------------------ MMA issuer (leader)
         MmaState ms;
-        for (int kind = kind0, i = 0; valid_at(kind, i); next_of(kind, i)) {
-          const int t = tile_at(i);
-          const bool ok = kind == GATE_UP ? mma_tile<GATE_UP>(h, p, ms, decode_tok(h, tb, nf1, g1, t), -1)
-                                          : mma_tile<DOWN>(h, p, ms, decode_tok(h, tb, nf2, g2, t), -1);
+        for (int n = 0;; ++n) {
+          const int c = tq_pop(h, p, tq, n);
+          if (c < 0) break;
+          const bool ok = kind_of(c) == GATE_UP ? mma_tile<GATE_UP>(h, p, ms, info_of(c), n)
+                                                : mma_tile<DOWN>(h, p, ms, info_of(c), n);
           if (!ok) break;
         }
         // after an abort the epilogue may stop before the last accumulator:
@@ -825,10 +815,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
       // -------------------------------------------------------------- epilogue
       const int q = wid & 3;  // TMEM lane quarter this warp may access
       EpiState es;
-      for (int kind = kind0, i = 0; valid_at(kind, i); next_of(kind, i)) {
-        const TileInfo ti = decode_tok(h, tb, kind == GATE_UP ? nf1 : nf2, kind == GATE_UP ? g1 : g2, tile_at(i));
-        const bool ok = kind == GATE_UP ? epi_tile<GATE_UP>(h, p, es, ti, -1, q, lane)
-                                        : epi_tile<DOWN>(h, p, es, ti, -1, q, lane);
+      for (int n = 0;; ++n) {
+        int c = 0;
+        if (lane == 0) c = tq_pop(h, p, tq, n);  // lane 0 reads the entry and hands it back
+        c = __shfl_sync(0xffffffffu, c, 0);
+        if (c < 0) break;
+        const TileInfo ti = info_of(c);
+        const bool ok = kind_of(c) == GATE_UP ? epi_tile<GATE_UP>(h, p, es, ti, n, q, lane)
+                                              : epi_tile<DOWN>(h, p, es, ti, n, q, lane);
         if (!ok) break;
         // publish this warp's share of the tile (read next by TMA or by the
         // combine's generic loads in other CTAs)
@@ -836,7 +830,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
         asm volatile("fence.proxy.async.global;" ::: "memory");
         __syncwarp();
         if (lane == 0)
-          atomicAdd((kind == GATE_UP ? h_ready(h) : y_ready(h)) + tb.tokprefix[ti.e] + ti.n, 1u);
+          atomicAdd((kind_of(c) == GATE_UP ? h_ready(h) : y_ready(h)) + tb.tokprefix[ti.e] + ti.n, 1u);
       }
     }
     if (*abort_s) set_abort(h);
@@ -891,6 +885,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
       c[C_SCATTER_NEXT] = 0;
       c[C_SCATTER_DONE] = 0;
       c[C_COMB_NEXT] = 0;
+      c[C_TILE_NEXT] = 0;
       c[C_ABORT] = 0;
       __threadfence();
       c[C_EXIT] = 0;

@@ -400,6 +400,158 @@ struct Pipe {
   int shard_direct = 0;
 };
 
+// ---------------------------------------------------------------------------
+// Dynamic tile schedule of a CTA pair (expert GEMM kinds).  The leader's
+// producer claims the next tile index from a global counter (one atomicAdd per
+// tile) just before it streams that tile, so a pair that finishes early takes
+// more tiles and the pairs end within about one tile of each other; under a
+// static assignment a launch ends with its slowest pair, and tiles differ in
+// cost with their row counts.  Consecutive claims are consecutive tiles, so
+// the pairs running at one time still share weight rows as a wave does.  The
+// index reaches the pair's other roles through a queue of TQ entries held in
+// both CTAs' shared memory: full[i] (in each CTA: the leader producer's one
+// arrival, after it wrote the entry there) and empty[i] (in the leader: one
+// arrival per consumer -- the peer's producer, the leader's MMA thread and the
+// 8 epilogue warps -- after it read the entry).  Entry -1 ends the schedule.
+// ---------------------------------------------------------------------------
+constexpr int TQ = 4;
+constexpr int TQ_CONSUMERS = 10;
+struct TileQueue {
+  volatile int *id;  // [TQ]
+  uint64_t *full;    // [TQ]
+  uint64_t *empty;   // [TQ] (the leader's are used)
+};
+// one thread of each CTA, before the cluster barrier that precedes any use
+__device__ __forceinline__ void tq_init(const TileQueue &q) {
+  for (int i = 0; i < TQ; ++i) {
+    mbar_init(&q.full[i], 1);
+    mbar_init(&q.empty[i], TQ_CONSUMERS);
+  }
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (the entry may come from the other
+// CTA of the pair); a timeout raises SYM_STATUS_TIMEOUT.
+__device__ inline bool tq_wait(const sym_heap &h, const Pipe &p, uint64_t *bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = (uint64_t)p.tmo * 1000ull;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    if (*p.abort) return false;
+    if ((it & 15u) == 15u && globaltimer_ns() - t0 > limit) {
+      raise_status(h, SYM_STATUS_TIMEOUT);
+      return false;
+    }
+  }
+}
+// Leader producer: entry n of the pair's schedule is tile `id` (-1: the end).
+__device__ inline bool tq_push(const sym_heap &h, const Pipe &p, const TileQueue &q, int n, int id) {
+  const int i = n % TQ;
+  const uint32_t use = (uint32_t)(n / TQ);
+  if (!tq_wait(h, p, &q.empty[i], (use & 1u) ^ 1u)) return false;
+  q.id[i] = id;
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(map_to((const void *)&q.id[i], 1)), "r"(id) : "memory");
+  mbar_arrive(&q.full[i]);
+  mbar_arrive_remote(map_to(&q.full[i], 1));  // release.cluster: orders the store above
+  return true;
+}
+// A consumer's entry n: its tile (-1: the end; -2: the wait failed), the
+// entry handed back once read.
+__device__ inline int tq_pop(const sym_heap &h, const Pipe &p, const TileQueue &q, int n) {
+  const int i = n % TQ;
+  const uint32_t use = (uint32_t)(n / TQ);
+  if (!tq_wait(h, p, &q.full[i], use & 1u)) return -2;
+  const int id = q.id[i];
+  if (p.rank == 0) mbar_arrive(&q.empty[i]);
+  else mbar_arrive_remote(map_to(&q.empty[i], 0));
+  return id;
+}
+
+// The producers' walk of the dynamic schedule.  The leader claims one tile
+// ahead: while it streams tile c it holds the next claim, checks that tile's
+// inputs halfway through c (probe) and publishes it as soon as they are in
+// place, so the peer and the MMA learn it early and no check sits between two
+// tiles.  A published entry therefore means "inputs ready": the peer streams
+// it without checking again (the leader's acquire of the ready counters and
+// its cluster-scope release of the entry order the inputs before the peer's
+// loads).  claim() gives the next tile or -1; ready(c, block) checks tile c's
+// inputs (bounded when blocking); produce(c, n, probe) streams tile c as entry
+// n.  On a failure *stop = the entry where the pair stopped.  Returns false
+// after a failure.
+template <typename Claim, typename Ready, typename Produce>
+__device__ bool produce_schedule(const sym_heap &h, const Pipe &p, const TileQueue &q, volatile int *stop,
+                                 Claim claim, Ready ready, Produce produce) {
+  auto no_probe = []() {};
+  if (p.rank != 0) {
+    for (int n = 0;; ++n) {
+      const int c = tq_pop(h, p, q, n);
+      if (c == -2) {
+        *stop = n;
+        return false;
+      }
+      if (c < 0) return true;
+      fence_proxy_async();  // inputs written by generic stores, made visible by the leader's check
+      if (!produce(c, n, no_probe)) return false;
+    }
+  }
+  int c = claim();
+  if (c >= 0 && !ready(c, true)) {
+    raise_status(h, SYM_STATUS_TIMEOUT);
+    *stop = 0;
+    tq_push(h, p, q, 0, -1);
+    return false;
+  }
+  if (!tq_push(h, p, q, 0, c)) {
+    *stop = 0;
+    return false;
+  }
+  for (int n = 0; c >= 0; ++n) {
+    const int c_next = claim();
+    bool pushed = false, failed = false;
+    auto probe = [&]() {
+      if (c_next < 0 || ready(c_next, false)) {
+        if (tq_push(h, p, q, n + 1, c_next)) pushed = true;
+        else failed = true;
+      }
+    };
+    fence_proxy_async();  // inputs written by generic stores
+    if (!produce(c, n, probe)) {
+      *stop = n;
+      if (!pushed && !failed) tq_push(h, p, q, n + 1, -1);
+      return false;
+    }
+    if (failed) {
+      *stop = n + 1;
+      return false;
+    }
+    if (!pushed) {
+      if (c_next >= 0 && !ready(c_next, true)) {
+        raise_status(h, SYM_STATUS_TIMEOUT);
+        *stop = n + 1;
+        tq_push(h, p, q, n + 1, -1);
+        return false;
+      }
+      if (!tq_push(h, p, q, n + 1, c_next)) {
+        *stop = n + 1;
+        return false;
+      }
+    }
+    c = c_next;
+  }
+  return true;
+}
+
 // K blocks [kb0, kb1) of tile ti
 __device__ __forceinline__ void k_range(const Pipe &p, const TileInfo &ti, int nk, int &kb0, int &kb1) {
   kb0 = p.kb_per_split ? ti.ks * p.kb_per_split : 0;
