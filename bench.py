@@ -121,24 +121,31 @@ def algorithmic(cfg: dict, experts_hit: int) -> dict:
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle samples every 20 ms.  The sampler starts
+    before the warm-up (so the timed steps follow the warm-up with no idle
+    gap); mark() brackets the timed region on the host clock and the summary
+    keeps only the samples taken inside it."""
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.window = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
 
     def __exit__(self, *a):
         self.lines = []
@@ -151,18 +158,34 @@ class ClockSampler:
                 out, _ = self.proc.communicate()
             self.lines = [l for l in out.splitlines() if l.strip()]
 
+    @staticmethod
+    def _when(stamp: str):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp.strip(), fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
     def summary(self):
         if not getattr(self, "lines", None):
             return None
-        sm, mx, reasons = [], None, set()
+        sm, mx, power, reasons, outside = [], None, [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in self.lines:
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
+            if self.window is not None:
+                t = self._when(f[0])
+                if t is not None and not (self.window[0] <= t <= self.window[1]):
+                    outside += 1
+                    continue
             try:
                 sm.append(float(f[1]))
                 mx = float(f[2])
+                power.append(float(f[3]))
             except ValueError:
                 continue
             for nm, v in zip(names, f[5:9]):
@@ -171,8 +194,9 @@ class ClockSampler:
         if not sm:
             return None
         sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": sm[len(sm) // 2], "sm_min_mhz": sm[0], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None,
+                "interval_ms": 20}
 
 
 TRAFFIC_SOURCES = ("expert_ffn.cu", "gemm2sm.cuh", "symmoe_dev.cuh")
@@ -373,19 +397,21 @@ def time_steps(wl: Workload, stream, steps: int, warmup: int, fused: int, wif=Fa
         if ev:
             ev[nst].record(stream)
 
-    for _ in range(max(warmup, 3)):
-        step()
-    torch.cuda.synchronize()
-    assert heap.status(stream=stream) == 0, "device status word set during warm-up"
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        for _ in range(max(warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        assert heap.status(stream=stream) == 0, "device status word set during warm-up"
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
         ev0.record(stream)
         for i in range(steps):
             step(i)
         ev1.record(stream)
         torch.cuda.synchronize()
+        clk.mark(t0, time.time())
     barrier()
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), world, device)
     assert heap.status(stream=stream) == 0, "device status word set during the timed steps"

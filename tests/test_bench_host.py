@@ -59,3 +59,16 @@ def test_one_core_leg_restores_threads_and_affinity():
         assert (a @ a)[0, 0] == 64.0
     assert bench.blas_threads() == before_threads
     assert os.sched_getaffinity(0) == before_aff
+
+
+def test_clock_summary_keeps_only_the_timed_window():
+    c = bench.ClockSampler(0)
+    c.lines = ["2026/12/03 06:13:02.100, 2070, 2070, 500.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "2026/12/03 06:13:02.300, 1600, 2070, 580.2, 0x4, Not Active, Not Active, Not Active, Active",
+               "2026/12/03 06:13:03.300, 1500, 2070, 590.0, 0x4, Not Active, Not Active, Active, Active"]
+    c.mark(c._when("2026/12/03 06:13:02.050"), c._when("2026/12/03 06:13:02.350"))
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_min_mhz"] == 1600.0 and s["reasons"] == ["sw_power_cap"]
+    c.window = None                                  # no window: every sample counts
+    s = c.summary()
+    assert s["samples"] == 3 and "sw_thermal_slowdown" in s["reasons"] and s["sm_min_mhz"] == 1500.0
