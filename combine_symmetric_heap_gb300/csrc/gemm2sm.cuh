@@ -167,16 +167,21 @@ __device__ inline void build_tok_tables(const sym_heap &h, const TokTables &tb) 
 // Token tiles per group in a kind's tile order.  Inside an expert the tiles
 // run feature tile major, so one weight tile serves all the expert's token
 // tiles back to back; but each feature tile then sweeps all the expert's token
-// rows again, and for gate/up (K = H) a heavy expert's rows (up to N rows of
-// H bf16) can outgrow L2 and be re-read from DRAM per feature tile.  So the
-// gate/up token tiles go in groups whose rows fit GROUP_B_BYTES: group by
-// group, feature tile major inside a group.  An expert whose rows fit keeps
-// one group (the plain order); the down GEMM (K = I, small rows) keeps one.
+// rows again, and a heavy expert's rows can outgrow L2 and be re-read from
+// DRAM per feature tile.  So the token tiles go in groups: group by group,
+// feature tile major inside a group.  Gate/up (K = H): a group's rows fit
+// 48 MB.  Down (K = I, the rows are h): a group's rows fit 64 MB, so that a
+// wave of tiles touches about as many h tiles as weight tiles (Mixtral-like:
+// groups of 8 of an expert's 16 token tiles instead of all 16; the expert FFN
+// measured 1.5-2.7% faster at full clock, 1.1% under the power cap).  An
+// expert whose rows fit keeps one group (the plain order).
 constexpr long long GROUP_B_BYTES = 48ll << 20;
+constexpr long long GROUP_H_BYTES = 64ll << 20;
 __host__ __device__ inline int tok_group_of(const sym_heap &h, int kind) {
-  if (kind != GATE_UP) return 1 << 30;
-  const long long tile_b = (long long)BN * h.s.hidden * 2;
-  return (int)(GROUP_B_BYTES / tile_b) > 1 ? (int)(GROUP_B_BYTES / tile_b) : 1;
+  if (kind != GATE_UP && kind != DOWN) return 1 << 30;
+  const long long budget = kind == GATE_UP ? GROUP_B_BYTES : GROUP_H_BYTES;
+  const long long tile_b = (long long)BN * (kind == GATE_UP ? h.s.hidden : h.s.inter) * 2;
+  return (int)(budget / tile_b) > 1 ? (int)(budget / tile_b) : 1;
 }
 
 __device__ inline TileInfo decode_tok(const sym_heap &h, const TokTables &tb, int nf, int group, int t) {

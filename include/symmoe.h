@@ -46,6 +46,15 @@
  * intermediate size, E = experts, E/W experts per slot (expert e lives on
  * slot e / (E/W)), k = top-k.  Limits: E % W == 0, 1 <= k <= min(E, 32),
  * E <= 1024, H % 128 == 0, I % 128 == 0, H, I <= 65536.
+ *
+ * Accuracy: the expert FFN accumulates in fp32 on the tensor cores, whose
+ * additions into the accumulator truncate.  Against an exact (fp64)
+ * reference, bf16 outputs stay within 2e-2 * max(1, |ref|) per element and
+ * 1e-2 relative L2 for K = H or I up to 16384 with weights ~N(0, 0.02).  At
+ * K = 65536 with weights that large, |h| reaches ~200 and the truncation
+ * over 4096 MMAs moves a few y elements in 10^4 just past that per-element
+ * bound (relative L2 stays ~1e-3); the bound holds there for weights scaled
+ * like a trained layer (about 1/sqrt(H): gate/up ~N(0, 0.0025) was checked).
  */
 #ifndef SYMMOE_H
 #define SYMMOE_H

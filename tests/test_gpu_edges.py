@@ -193,6 +193,26 @@ def test_grouped_token_tiles(sm, fused):
 
 
 @pytest.mark.parametrize("fused", [0, 1])
+def test_grouped_down_tiles(sm, fused):
+    """Down token tiles of a heavy expert run in groups whose h rows fit a
+    fixed L2 budget (64 MiB: 8 token tiles of 256 rows at I = 16384): 2600
+    rows make 11 tiles (10 full, one of 40 rows) in groups of 8 and 3, and a
+    second expert of 90 rows keeps one short tile."""
+    counts = [2600, 90]
+    cfg = dict(world=1, tokens_per_slot=sum(counts), hidden=128, num_experts=2, topk=1, inter=16384)
+    idx = np.repeat(np.arange(len(counts)), counts).reshape(-1, 1)
+    idx = idx[np.random.default_rng(13).permutation(len(idx))]
+    w = np.ones_like(idx, dtype=np.float32)
+    heap, out, w_used = _run(sm, cfg, idx, w, fused)
+    assert heap.status() == 0
+    ref = _oracle_from_idx(cfg, idx, w_used, fresh_weight_fn(cfg, DEV))
+    assert ref["cnt"].tolist() == counts
+    t = int(ref["tot"][0])
+    assert_close(bits(heap.y(0)[:t]), ref["y_exact"][0], "grouped down tiles y")
+    assert_close(bits(out), bf16_f64(ref["out"]), "grouped down tiles out")
+
+
+@pytest.mark.parametrize("fused", [0, 1])
 @pytest.mark.parametrize("hidden,inter", [(65536, 128), (128, 65536)])
 def test_largest_hidden_and_inter(sm, fused, hidden, inter):
     """The ABI's largest H and I: a dispatched / combined row of 8192 16-byte
