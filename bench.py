@@ -505,11 +505,11 @@ def stage_bandwidth(cfg: dict, stages: dict, fused: int) -> dict:
 
 
 def workload_summary(name: str, cfg: dict, fused: int, steps: int, ms_total: float, stages: dict,
-                     clocks, counts) -> dict:
+                     clocks, counts, start: str = "from idle") -> dict:
     """One entry of the per-workload record."""
     n = cfg["world"] * cfg["tokens_per_slot"]
     rl = roofline_of(cfg, counts, stages, fused, ms_total)
-    return {"workload": name, "fused": bool(fused), "steps": steps,
+    return {"workload": name, "fused": bool(fused), "steps": steps, "start": start,
             "tokens_per_s": n * steps / (ms_total / 1e3), "ms_per_step": ms_total / steps,
             "stages_ms": stages, "ffn_roof": {k: rl[k] for k in ("bound", "achieved", "peak", "unit", "frac",
                                                                  "peak_kind", "per_expert_roof", "other_roof")},
@@ -692,6 +692,9 @@ def run_e2e_loop(wl: Workload, stream, steps: int, fused: int, wif: bool, dedup:
             "overlap": "uploads and downloads on their own streams, double-buffered"}
 
 
+IDLE_BETWEEN_S = 1.5
+
+
 def run_per_workload(sm, head: Workload, args, stream, world, local, barrier, dev, head_fused, head_stages,
                      head_ms, head_clocks, head_counts) -> list:
     """Every configuration of the path in one run: the headline workload's
@@ -703,7 +706,14 @@ def run_per_workload(sm, head: Workload, args, stream, world, local, barrier, de
     import moe_synth as ms
     steps = args.steps
     rec = [workload_summary(args.config, head.cfg, head_fused, steps, head_ms, head_stages, head_clocks,
-                            head_counts)]
+                            head_counts, start="the headline's own timed steps")]
+    # Every entry starts from the state the headline started from: an idle GPU
+    # (the headline's timed steps follow only input generation and a short
+    # warm-up).  Back-to-back load engages the power cap within ~0.25 s and
+    # lowers the SM clock by up to a quarter; the clocks sampled during each
+    # entry's timed steps are recorded beside it.
+    idle = lambda: time.sleep(IDLE_BETWEEN_S)
+    idle()
     ms_total, st, clk = time_steps(head, stream, steps, args.warmup, 1 - head_fused, world=world, local=local,
                                    barrier=barrier, device=dev)
     rec.append(workload_summary(args.config, head.cfg, 1 - head_fused, steps, ms_total, st, clk,
@@ -719,6 +729,8 @@ def run_per_workload(sm, head: Workload, args, stream, world, local, barrier, de
         wl = Workload(sm, cfg, dev, weights=shared[key])
         forms = (1, 0) if cfg.get("fused") else (0, 1)
         for f in forms:
+            torch.cuda.synchronize()
+            idle()
             ms_total, st, clk = time_steps(wl, stream, steps, args.warmup, f, world=world, local=local,
                                            barrier=barrier, device=dev)
             rec.append(workload_summary(name, cfg, f, steps, ms_total, st, clk, expert_counts(wl.heap, cfg)))
