@@ -15,9 +15,9 @@
 //   count   one CTA per 128-token chunk: per-expert bitmask of the chunk's
 //           tokens in shared memory -> each pair's rank inside the chunk
 //           (popcount of the lower bits) and the chunk histogram.
-//   scan    one CTA: exclusive scan of the chunk histograms per expert (warp
-//           scans), expert counts, receive offsets per slot, total rows per
-//           slot; clears the ready counters for this call.
+//   scan    one CTA per slot: exclusive scan of the chunk histograms of the
+//           slot's experts (a warp per expert), expert counts, receive
+//           offsets, total rows; clears the slot's ready counters.
 //   scatter one 64-thread CTA per token: x[g] is read once and stored k times
 //           (one per destination), then recv_pair / recv_w / pos are written
 //           and the ready counter of each destination row block is raised.
@@ -81,19 +81,23 @@ __global__ void __launch_bounds__(CHUNK) dispatch_count_kernel(sym_heap h,
   }
 }
 
+// One CTA per slot: a slot's receive offsets depend only on its own experts.
+// A warp per expert scans the expert's chunk histogram row (warp scans, 32
+// chunks at a time), then the slot's counts, offsets and total are written
+// and its ready counters cleared for this call.
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(sym_heap h) {
   __shared__ int32_t cnt_s[1024];
   const int E = h.s.num_experts, W = h.s.world;
   const int E_loc = E / W;
+  const int d = blockIdx.x;
   const int N = W * h.s.tokens_per_slot;
   const int nchunks = (N + CHUNK - 1) / CHUNK;
   int32_t *hist = win<int32_t>(h, 0, h.off_hist);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   pdl_launch_dependents();
   pdl_wait();  // the count kernel's histogram
-  // per expert: exclusive scan over chunks (warp scan, 32 chunks at a time)
-  for (int e = wid; e < E; e += nw) {
-    int32_t *row = hist + (size_t)e * nchunks;
+  for (int l = wid; l < E_loc; l += nw) {
+    int32_t *row = hist + (size_t)(d * E_loc + l) * nchunks;
     int carry = 0;
     for (int c0 = 0; c0 < nchunks; c0 += 32) {
       const int c = c0 + lane;
@@ -107,19 +111,17 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(sym_heap h) {
       if (c < nchunks) row[c] = carry + incl - v;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) cnt_s[e] = carry;
+    if (lane == 0) cnt_s[l] = carry;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int d = e / E_loc, l = e % E_loc;
+  for (int l = threadIdx.x; l < E_loc; l += blockDim.x) {
     int off = 0;
-    for (int i = 0; i < l; ++i) off += cnt_s[d * E_loc + i];
-    win<int32_t>(h, d, h.off_cnt)[l] = cnt_s[e];
+    for (int i = 0; i < l; ++i) off += cnt_s[i];
+    win<int32_t>(h, d, h.off_cnt)[l] = cnt_s[l];
     win<int32_t>(h, d, h.off_recv_off)[l] = off;
-    if (l == E_loc - 1) *win<int32_t>(h, d, h.off_total) = off + cnt_s[e];
+    if (l == E_loc - 1) *win<int32_t>(h, d, h.off_total) = off + cnt_s[l];
   }
-  for (int i = threadIdx.x; i < W * (int)h.num_ready; i += blockDim.x)
-    win<uint32_t>(h, i / h.num_ready, h.off_ready)[i % h.num_ready] = 0u;
+  for (int i = threadIdx.x; i < (int)h.num_ready; i += blockDim.x) win<uint32_t>(h, d, h.off_ready)[i] = 0u;
 }
 
 // Scatter: a CTA of 64 threads per token, each thread holding VEC 16-byte
@@ -565,7 +567,9 @@ cudaError_t launch_dispatch(const sym_heap &h, const uint16_t *x, const int32_t 
   if (err != cudaSuccess) return err;
   // scan and scatter are scheduled while their predecessor drains (they wait
   // for its results on the device)
-  if ((err = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(1024), 0, st, h)) != cudaSuccess) return err;
+  const int scan_threads = std::min(1024, 32 * (h.s.num_experts / h.s.world));
+  if ((err = launch_pdl(dispatch_scan_kernel, dim3(h.s.world), dim3(scan_threads), 0, st, h)) != cudaSuccess)
+    return err;
   // vectors per thread: the whole row in one pass up to H = 8192
   const int nvec = h.s.hidden / 8;
   if (mode == 2) {
