@@ -360,6 +360,38 @@ def test_pipeline_full_size_sampled(sm, name, ntok, maxe):
         assert_close(bits(out[g]), bf16_f64(ref_out), f"{name} token {g}")
 
 
+@pytest.mark.slow
+def test_skewed_heaviest_expert_every_element(sm):
+    """The full Skewed workload (Zipf-biased routing): every h and y element of
+    its heaviest expert (thousands of rows: many token tiles, gate/up token
+    groups, a ragged last tile) against the oracle, and its received rows
+    bit-exact."""
+    cfg = ms.CONFIGS["skewed"]
+    n, k, E, W = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"], cfg["num_experts"], cfg["world"]
+    logits, x, wg, wu, wd = device_inputs(cfg, DEV)
+    heap = sm.SymHeap(cfg, DEV)
+    idx = torch.empty((n, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((n, k), dtype=torch.float32, device=DEV)
+    out = torch.empty((n, cfg["hidden"]), dtype=torch.bfloat16, device=DEV)
+    heap.pipeline(logits, x, wg, wu, wd, idx, w, out, fused=0)
+    torch.cuda.synchronize()
+    assert heap.status() == 0
+    del wg, wu, wd, x
+    torch.cuda.empty_cache()
+    ridx, _ = oracle.route_topk(ms.logits_np(cfg), k)
+    cnt, off, _ = oracle.count_experts(ridx, E, W)
+    e = int(np.argmax(cnt))
+    d, o, c = e // (E // W), int(off[e]), int(cnt[e])
+    assert c > 8 * 256                       # many token tiles
+    tokens = np.nonzero((ridx == e).any(axis=1))[0]   # its rows, in receive order
+    assert len(tokens) == c
+    rows = bits(ms.x_torch(cfg, DEV)[torch.from_numpy(tokens).to(DEV)])
+    assert np.array_equal(bits(heap.recv_x(d)[o:o + c]), rows)
+    h_bits, _, y_exact = oracle.expert_ffn_rows(rows, *fresh_weight_fn(cfg, DEV)(e))
+    assert_close(bits(heap.h(d)[o:o + c]), bf16_f64(h_bits), f"skewed expert {e} h ({c} rows)")
+    assert_close(bits(heap.y(d)[o:o + c]), y_exact, f"skewed expert {e} y ({c} rows)")
+
+
 # ----------------------------------------------------------------- bounded waits
 
 def test_ready_counter_timeout_returns_with_status(sm):
