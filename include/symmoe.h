@@ -34,7 +34,10 @@
  *     events per device, created on first use and kept for the process.
  *   - bf16 tensors are passed as uint16_t bit patterns, row-major, contiguous.
  *   - All compute calls are asynchronous on `stream` (a cudaStream_t; NULL is
- *     the legacy default stream) and never synchronise the host.
+ *     the legacy default stream) and never synchronise the host.  Calls on
+ *     one heap must run one after another on the GPU (one stream, or streams
+ *     ordered by events): they share its windows and the work counters in
+ *     its control window, which every launch leaves at zero when it ends.
  *   - Return value: SYM_OK (0) or a negative SYM_E* code, detected
  *     synchronously (bad argument, too small a heap, launch failure).
  *     Conditions found on the device while a kernel runs (a bounded wait that
