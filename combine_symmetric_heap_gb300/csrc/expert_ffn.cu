@@ -133,7 +133,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       auto produce = [&](int t, int n, auto &probe) {
         return produce_tile<KIND>(h, p, ps, decode_tok(h, tb, nf, grp, t), &tm_a0, &tm_a1, tm_b, n, probe);
       };
-      produce_schedule(h, p, tq, stop_tile, claim, ready, produce);
+      produce_schedule(h, p, tq, stop_tile, wait_ready != 0, claim, ready, produce);
     }
   } else if (wid == 1) {
     if (lane == 0 && p.rank == 0) {

@@ -793,7 +793,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
                      ? produce_tile<GATE_UP>(h, p, ps, info_of(c), &tm_g, &tm_u, tm_rx, n, probe)
                      : produce_tile<DOWN>(h, p, ps, info_of(c), &tm_d, &tm_d, tm_h, n, probe);
         };
-        if (!produce_schedule(h, p, tq, never_s, claim, ready, produce)) *abort_s = 1;
+        if (!produce_schedule(h, p, tq, never_s, true, claim, ready, produce)) *abort_s = 1;
       }
     } else if (wid == 1) {
       if (lane == 0 && p.rank == 0) {

@@ -492,11 +492,13 @@ __device__ inline int tq_pop(const sym_heap &h, const Pipe &p, const TileQueue &
 // its cluster-scope release of the entry order the inputs before the peer's
 // loads).  claim() gives the next tile or -1; ready(c, block) checks tile c's
 // inputs (bounded when blocking); produce(c, n, probe) streams tile c as entry
-// n.  On a failure *stop = the entry where the pair stopped.  Returns false
-// after a failure.
+// n.  fence_inputs: the inputs may have been written by generic stores during
+// this launch or one overlapping it (a proxy fence then precedes each tile's
+// loads); inputs written by an earlier kernel need none.  On a failure *stop
+// = the entry where the pair stopped.  Returns false after a failure.
 template <typename Claim, typename Ready, typename Produce>
 __device__ bool produce_schedule(const sym_heap &h, const Pipe &p, const TileQueue &q, volatile int *stop,
-                                 Claim claim, Ready ready, Produce produce) {
+                                 bool fence_inputs, Claim claim, Ready ready, Produce produce) {
   auto no_probe = []() {};
   if (p.rank != 0) {
     for (int n = 0;; ++n) {
@@ -506,7 +508,7 @@ __device__ bool produce_schedule(const sym_heap &h, const Pipe &p, const TileQue
         return false;
       }
       if (c < 0) return true;
-      fence_proxy_async();  // inputs written by generic stores, made visible by the leader's check
+      if (fence_inputs) fence_proxy_async();  // made visible by the leader's check
       if (!produce(c, n, no_probe)) return false;
     }
   }
@@ -530,7 +532,7 @@ __device__ bool produce_schedule(const sym_heap &h, const Pipe &p, const TileQue
         else failed = true;
       }
     };
-    fence_proxy_async();  // inputs written by generic stores
+    if (fence_inputs) fence_proxy_async();  // inputs written by generic stores
     if (!produce(c, n, probe)) {
       *stop = n;
       if (!pushed && !failed) tq_push(h, p, q, n + 1, -1);
