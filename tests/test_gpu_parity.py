@@ -360,14 +360,11 @@ def test_pipeline_full_size_sampled(sm, name, ntok, maxe):
         assert_close(bits(out[g]), bf16_f64(ref_out), f"{name} token {g}")
 
 
-@pytest.mark.slow
-def test_skewed_heaviest_expert_every_element(sm):
-    """The full Skewed workload (Zipf-biased routing): every h and y element of
-    its heaviest expert (thousands of rows: many token tiles, gate/up token
-    groups, a ragged last tile) against the oracle, and its received rows
-    bit-exact."""
-    cfg = ms.CONFIGS["skewed"]
-    n, k, E, W = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"], cfg["num_experts"], cfg["world"]
+def _full_size_run(sm, name):
+    """The full workload through the staged pipeline; returns the heap and the
+    oracle's routing of the same logits (bit-exact against the launch's)."""
+    cfg = ms.CONFIGS[name]
+    n, k = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"]
     logits, x, wg, wu, wd = device_inputs(cfg, DEV)
     heap = sm.SymHeap(cfg, DEV)
     idx = torch.empty((n, k), dtype=torch.int32, device=DEV)
@@ -379,17 +376,59 @@ def test_skewed_heaviest_expert_every_element(sm):
     del wg, wu, wd, x
     torch.cuda.empty_cache()
     ridx, _ = oracle.route_topk(ms.logits_np(cfg), k)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    return cfg, heap, ridx
+
+
+def _expert_every_element(cfg, heap, ridx, e, what):
+    """Every h and y element of expert e against the oracle, its received
+    rows bit-exact."""
+    E, W = cfg["num_experts"], cfg["world"]
     cnt, off, _ = oracle.count_experts(ridx, E, W)
-    e = int(np.argmax(cnt))
     d, o, c = e // (E // W), int(off[e]), int(cnt[e])
-    assert c > 8 * 256                       # many token tiles
     tokens = np.nonzero((ridx == e).any(axis=1))[0]   # its rows, in receive order
     assert len(tokens) == c
     rows = bits(ms.x_torch(cfg, DEV)[torch.from_numpy(tokens).to(DEV)])
     assert np.array_equal(bits(heap.recv_x(d)[o:o + c]), rows)
     h_bits, _, y_exact = oracle.expert_ffn_rows(rows, *fresh_weight_fn(cfg, DEV)(e))
-    assert_close(bits(heap.h(d)[o:o + c]), bf16_f64(h_bits), f"skewed expert {e} h ({c} rows)")
-    assert_close(bits(heap.y(d)[o:o + c]), y_exact, f"skewed expert {e} y ({c} rows)")
+    assert_close(bits(heap.h(d)[o:o + c]), bf16_f64(h_bits), f"{what}: expert {e} h ({c} rows)")
+    assert_close(bits(heap.y(d)[o:o + c]), y_exact, f"{what}: expert {e} y ({c} rows)")
+    return c
+
+
+@pytest.mark.slow
+def test_skewed_heaviest_expert_every_element(sm):
+    """The full Skewed workload (Zipf-biased routing): every h and y element of
+    its heaviest expert (thousands of rows: many token tiles, gate/up token
+    groups, a ragged last tile) against the oracle, and its received rows
+    bit-exact."""
+    cfg, heap, ridx = _full_size_run(sm, "skewed")
+    cnt, _, _ = oracle.count_experts(ridx, cfg["num_experts"], cfg["world"])
+    assert _expert_every_element(cfg, heap, ridx, int(np.argmax(cnt)), "skewed") > 8 * 256
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mixtral", "deepseek", "decode"])
+def test_full_size_experts_every_element(sm, name):
+    """Every h and y element of chosen experts of the full workloads against the
+    oracle: Mixtral-like's last expert (~4096 rows: 16 token tiles, the down
+    tiles in two groups); DeepSeek-like's largest expert with 257..288 rows (the
+    remainder on its one tile as a second MMA) and its largest with at most 256;
+    Decode's largest expert (a few dozen rows, one short tile)."""
+    cfg, heap, ridx = _full_size_run(sm, name)
+    E = cfg["num_experts"]
+    cnt, _, _ = oracle.count_experts(ridx, E, cfg["world"])
+    if name == "mixtral":
+        chosen = [E - 1]
+    elif name == "deepseek":
+        fold = [e for e in range(E) if 256 < cnt[e] <= 288]
+        plain = [e for e in range(E) if 0 < cnt[e] <= 256]
+        assert fold and plain
+        chosen = [max(fold, key=lambda e: cnt[e]), max(plain, key=lambda e: cnt[e])]
+    else:
+        chosen = [int(np.argmax(cnt))]
+    for e in chosen:
+        _expert_every_element(cfg, heap, ridx, e, name)
 
 
 # ----------------------------------------------------------------- bounded waits
