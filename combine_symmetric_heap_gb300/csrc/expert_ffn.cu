@@ -152,7 +152,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       int t = 0;
       if (lane == 0) t = tq_pop(h, p, tq, n);  // lane 0 reads the entry and hands it back
       t = __shfl_sync(0xffffffffu, t, 0);
-      if (t < 0 || !epi_tile<KIND>(h, p, es, decode_tok(h, tb, nf, grp, t), n, q, lane)) break;
+      // The gate/up epilogue's partner warps meet at named barriers, so they
+      // act on an entry only together: they read the same entries, but a
+      // failed wait (an abort in this CTA) can end one partner's read early.
+      if (KIND == GATE_UP ? !xch_vote(q & 1, t >= 0) : t < 0) break;
+      if (!epi_tile<KIND>(h, p, es, decode_tok(h, tb, nf, grp, t), n, q, lane)) break;
     }
   }
 

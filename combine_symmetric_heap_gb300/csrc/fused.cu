@@ -425,6 +425,7 @@ __device__ inline void combine_token(const sym_heap &h, const FusedArgs &a, cons
     src_s[lane] = src;
     w_s[lane] = a.weights_in_ffn ? 1.f : __ldcg(a.w + (size_t)g * k + lane);
   }
+  __syncwarp();  // the tables are read by every lane below
   if (!__all_sync(0xffffffffu, ok)) return;
   uint4 *dst = reinterpret_cast<uint4 *>(a.out) + (size_t)g * (H / 8);
   const int nvec = H / 8;
@@ -505,6 +506,7 @@ __device__ inline void combine_token_stream(const sym_heap &h, const FusedArgs &
     src_s[lane] = src;
     w_s[lane] = a.weights_in_ffn ? 1.f : __ldcg(a.w + (size_t)g * k + lane);
   }
+  __syncwarp();  // the tables are read by every lane below
   if (!__all_sync(0xffffffffu, ok)) return;
   uint4 *dst = reinterpret_cast<uint4 *>(a.out) + (size_t)g * (H / 8);
   const int nvec = H / 8, step = 32 * U;
@@ -819,7 +821,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_THREADS, 1)
         int c = 0;
         if (lane == 0) c = tq_pop(h, p, tq, n);  // lane 0 reads the entry and hands it back
         c = __shfl_sync(0xffffffffu, c, 0);
-        if (c < 0) break;
+        // The gate/up epilogue's partner warps meet at named barriers, so they
+        // act on an entry only together: they read the same entries, but a
+        // failed wait (an abort in this CTA) can end one partner's read early.
+        if (!xch_vote(q & 1, c >= 0)) break;
         const TileInfo ti = info_of(c);
         const bool ok = kind_of(c) == GATE_UP ? epi_tile<GATE_UP>(h, p, es, ti, n, q, lane)
                                               : epi_tile<DOWN>(h, p, es, ti, n, q, lane);
