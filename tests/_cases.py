@@ -7,6 +7,7 @@ import numpy as np
 import torch
 
 import moe_synth as ms
+import oracle
 
 # Float tolerance for bf16 outputs against the fp64 oracle: per element
 # |gpu - ref| <= 2e-2 * max(1, |ref|), and relative L2 over the tensor <= 1e-2.
@@ -24,6 +25,23 @@ SMALL = {
     # k = 1, ~300 rows per expert: two token tiles (256 + ragged) per expert
     "multi": dict(world=1, tokens_per_slot=600, hidden=128, num_experts=2, topk=1, inter=256),
 }
+
+
+# routing weights: fp32 expf on the GPU against the fp64 oracle
+W_TOL = 2e-6
+
+
+def checked_oracle_routing(cfg: dict, idx: torch.Tensor, w: torch.Tensor | None = None, seed: int = 0):
+    """The oracle's routing of the generator's logits for ``cfg``.  The CUDA
+    path's routing of the same logits (``idx``, ``w``) must match it: indices
+    bit-exact, weights within W_TOL.  Returns the oracle's indices and
+    weights (never the launch's) for the oracle calls that follow."""
+    ridx, rw = oracle.route_topk(ms.logits_np(cfg, seed), cfg["topk"])
+    assert np.array_equal(idx.cpu().numpy(), ridx), "routing indices differ from the oracle's"
+    if w is not None:
+        err = np.abs(w.cpu().numpy().astype(np.float64) - rw.astype(np.float64)).max(initial=0.0)
+        assert err <= W_TOL, f"routing weights: max error {err}"
+    return ridx, rw
 
 
 def bits(t: torch.Tensor) -> np.ndarray:

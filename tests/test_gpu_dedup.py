@@ -8,7 +8,7 @@ import torch
 
 import moe_synth as ms
 import oracle
-from _cases import SMALL, bits
+from _cases import SMALL, bits, checked_oracle_routing
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -65,9 +65,10 @@ def test_dedup_matches_plain_and_oracle(sm, name):
             else:
                 assert torch.equal(a[d][key], b[d][key]), (name, d, key)
     # staging rows and row sources against the oracle
-    idx_h = idx.cpu().numpy()
+    # the oracle's own routing of the same logits (the launch's must equal it)
+    idx_h, w_h = checked_oracle_routing(cfg, idx, w)
     toks = oracle.dedup_tokens(idx_h, E, W)
-    pos, _, _ = oracle.place_pairs(idx_h, w.cpu().numpy(), E, W)
+    pos, _, _ = oracle.place_pairs(idx_h, w_h, E, W)
     src = oracle.dedup_row_source(idx_h, E, W, pos)
     x_h = ms.x_np(cfg)
     for d in range(W):

@@ -9,7 +9,7 @@ import torch
 
 import moe_synth as ms
 import oracle
-from _cases import SMALL, assert_close, bits, bf16_f64, fresh_weight_fn
+from _cases import SMALL, assert_close, bits, bf16_f64, checked_oracle_routing, fresh_weight_fn
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -36,10 +36,10 @@ def _dispatch(sm, cfg, x, fp8, idx=None):
     return heap, idx, w
 
 
-def _check_slots(heap, cfg, idx, x_bits):
-    """codes, scales and dequantized rows of every received row vs the oracle"""
+def _check_slots(heap, cfg, idx_h, x_bits):
+    """codes, scales and dequantized rows of every received row vs the oracle;
+    idx_h: the routing as the test or the oracle made it (host array)"""
     E, W, k, H = cfg["num_experts"], cfg["world"], cfg["topk"], cfg["hidden"]
-    idx_h = idx.cpu().numpy()
     pos, rp, _ = oracle.place_pairs(idx_h, np.ones(idx_h.shape, np.float32), E, W)
     codes, exps = oracle.quantize_rows_e4m3(x_bits)
     deq = oracle.dequantize_rows(codes, exps)
@@ -58,7 +58,7 @@ def test_fp8_dispatch_small(sm, name):
     cfg = SMALL[name]
     x = ms.x_torch(cfg, DEV)
     heap, idx, w = _dispatch(sm, cfg, x, True)
-    _check_slots(heap, cfg, idx, ms.x_np(cfg))
+    _check_slots(heap, cfg, checked_oracle_routing(cfg, idx, w)[0], ms.x_np(cfg))
     plain, _, _ = _dispatch(sm, cfg, x, False)
     for d in range(cfg["world"]):
         t = int(plain.total_recv(d).item())
@@ -88,9 +88,9 @@ def test_fp8_rounding_edges(sm):
         rows.append(v * scale)
     xb = oracle.round_f64_to_bf16_bits(np.array(rows))
     x = torch.from_numpy(xb.view(np.int16)).to(DEV).view(torch.bfloat16)
-    idx = torch.zeros((6, 1), dtype=torch.int32, device=DEV)
-    heap, idx, _ = _dispatch(sm, cfg, x, True, idx=idx)
-    _check_slots(heap, cfg, idx, xb)
+    idx_h = np.zeros((6, 1), dtype=np.int32)
+    heap, _, _ = _dispatch(sm, cfg, x, True, idx=torch.from_numpy(idx_h).to(DEV))
+    _check_slots(heap, cfg, idx_h, xb)
 
 
 def test_fp8_pipeline_matches_oracle_on_dequantized_rows(sm):
@@ -119,7 +119,7 @@ def test_fp8_dispatch_full_size_sampled(sm, name):
     E, W, k, H = cfg["num_experts"], cfg["world"], cfg["topk"], cfg["hidden"]
     x = ms.x_torch(cfg, DEV)
     heap, idx, w = _dispatch(sm, cfg, x, True)
-    idx_h = idx.cpu().numpy()
+    idx_h, _ = checked_oracle_routing(cfg, idx, w)
     pos = np.stack([heap.pos(d).cpu().numpy().reshape(-1, k) for d in range(W)]).reshape(-1, k)
     rng = np.random.default_rng(12)
     toks = np.sort(rng.choice(idx_h.shape[0], size=24, replace=False))

@@ -17,7 +17,8 @@ import torch
 
 import moe_synth as ms
 import oracle
-from _cases import assert_canaries, assert_close, bits, device_inputs, fresh_weight_fn, plant_canaries
+from _cases import (assert_canaries, assert_close, bits, checked_oracle_routing, device_inputs, fresh_weight_fn,
+                    plant_canaries)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -63,14 +64,19 @@ def test_expert_rows_past_capacity_are_skipped(sm, excess):
     assert_canaries(heap, "expert FFN with a count past capacity")
     # the skipped expert stored nothing; every other expert matches the oracle
     assert int((heap.y(d)[o:o + c].view(torch.int16) != 0).sum()) == 0
+    # every other expert against the oracle, on the oracle's own routing and
+    # placement of the same logits (the launch's routing must equal it)
+    ridx, rw = checked_oracle_routing(CFG, idx, w)
+    E, W, k = CFG["num_experts"], CFG["world"], CFG["topk"]
+    cnt, off, _ = oracle.count_experts(ridx, E, W)
+    _, rp, _ = oracle.place_pairs(ridx, rw, E, W)
     wfn = fresh_weight_fn(CFG, DEV)
     x_bits = ms.x_np(CFG)
-    rp = [heap.recv_pair(s).cpu().numpy() for s in range(CFG["world"])]
-    for e in range(CFG["num_experts"]):
+    for e in range(E):
         if e == e_bad:
             continue
-        s, oe, ce = _y_of_expert(heap, e, e_loc)
-        rows = x_bits[rp[s][oe:oe + ce] // CFG["topk"]]
+        s, oe, ce = e // e_loc, int(off[e]), int(cnt[e])
+        rows = x_bits[rp[s][oe:oe + ce] // k]
         _, _, ye = oracle.expert_ffn_rows(rows, *wfn(e))
         assert_close(bits(heap.y(s)[oe:oe + ce]), ye, f"expert {e} y")
 

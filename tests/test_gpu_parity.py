@@ -7,8 +7,8 @@ import torch
 
 import moe_synth as ms
 import oracle
-from _cases import (SMALL, assert_close, bf16_f64, bits, device_inputs, fresh_weight_fn,
-                    host_weight_fn, run_gpu_stages)
+from _cases import (SMALL, W_TOL, assert_close, bf16_f64, bits, checked_oracle_routing, device_inputs,
+                    fresh_weight_fn, host_weight_fn, run_gpu_stages)
 
 pytestmark = pytest.mark.gpu
 
@@ -87,8 +87,9 @@ def _check_dispatch(sm, cfg, heap, idx, w, x_dev, sample_rows=None):
     W, E, k = cfg["world"], cfg["num_experts"], cfg["topk"]
     e_loc = E // W
     T = cfg["tokens_per_slot"]
-    idx_h = idx.cpu().numpy()
-    w_h = w.cpu().numpy()
+    # the oracle's own routing of the same logits; the launch's must equal it
+    idx_h, w_h = checked_oracle_routing(cfg, idx, w)
+    w_gpu = w.cpu().numpy().reshape(-1)
     cnt, off, tot = oracle.count_experts(idx_h, E, W)
     pos, rp, rw = oracle.place_pairs(idx_h, w_h, E, W)
     g_cnt = np.concatenate([heap.cnt(d).cpu().numpy() for d in range(W)])
@@ -102,7 +103,9 @@ def _check_dispatch(sm, cfg, heap, idx, w, x_dev, sample_rows=None):
     for d in range(W):
         t = int(tot[d])
         assert np.array_equal(heap.recv_pair(d)[:t].cpu().numpy(), rp[d])
-        assert np.array_equal(heap.recv_w(d)[:t].cpu().numpy(), rw[d])
+        # each row's weight is a bit copy of its pair's routing weight
+        assert np.array_equal(heap.recv_w(d)[:t].cpu().numpy(), w_gpu[rp[d]])
+        assert np.abs(heap.recv_w(d)[:t].cpu().numpy().astype(np.float64) - rw[d]).max(initial=0.0) <= W_TOL
         # every received row is a bit copy of its source token (any size)
         src = torch.from_numpy(rp[d] // k).to(DEV)
         assert torch.equal(heap.recv_x(d)[:t].view(torch.int16), x_dev[src].view(torch.int16))
