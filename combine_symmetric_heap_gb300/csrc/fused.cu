@@ -927,7 +927,7 @@ cudaError_t launch_fused(const sym_heap &h, const float *logits, const uint16_t 
   cudaError_t err = cudaFuncSetAttribute(moe_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
   if (err != cudaSuccess) return err;
-  // every pair resident at once: phase 3 assigns tiles to pairs statically
+  // every pair resident at once: a down tile waits for gate/up tiles that other pairs hold
   const int grid = 2 * max_resident_pairs((const void *)moe_fused_kernel, FUSED_THREADS, smem, num_sms);
   if (grid <= 0) return cudaErrorInvalidConfiguration;
   const FusedArgs a{logits, x, idx, w, out, weights_in_ffn};
