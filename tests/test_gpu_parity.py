@@ -56,7 +56,7 @@ def test_route_parity(sm, name):
     heap = sm.SymHeap(small, DEV)
     heap.route_topk(lg, idx, w)
     torch.cuda.synchronize()
-    ridx, rw = oracle.route_topk(lg.cpu().numpy(), k)
+    ridx, rw = oracle.route_topk(ms.logits_np(cfg), k)  # the generator's host copy of the same logits
     assert np.array_equal(idx.cpu().numpy(), ridx)
     assert np.max(np.abs(w.cpu().numpy().astype(np.float64) - rw)) <= 2e-6
 
