@@ -1,6 +1,7 @@
 // gemm2sm.cuh -- the expert GEMM tiles on CTA pairs (tcgen05 cta_group::2):
 // one M=256 MMA spans the tensor cores of two SMs of a cluster.  Used by the
-// staged expert FFN and by the fused pipeline.
+// staged expert FFN and by the fused pipeline, and, as two more tile kinds,
+// by the router GEMM and the linear layer of the GEMM + all-to-all workload.
 //
 // Each CTA of the pair stages only its half of both operands: 128 of the 256
 // weight rows (A) and N/2 of the N token rows (B); the MMA, issued by the
@@ -354,7 +355,9 @@ __device__ __forceinline__ void commit2_both(uint64_t *bar) {
 }
 
 
-// Static pair schedule over a list of tiles: wave i holds tiles
+// Static pair schedule, for the router and the linear-layer kernels, whose
+// tiles all cost about the same (the expert GEMM's tiles differ with their
+// row counts and are claimed dynamically, below).  Wave i holds tiles
 // [i*npairs, (i+1)*npairs) (consecutive tiles share weight rows, so a wave
 // streams each weight block from HBM about once); pair p takes tile
 // i*npairs + (p+i) mod npairs of it.  The rotation keeps tiles that recur
