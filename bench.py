@@ -202,25 +202,54 @@ class ClockSampler:
 TRAFFIC_SOURCES = ("expert_ffn.cu", "gemm2sm.cuh", "symmoe_dev.cuh")
 
 
-def sources_sha256(files=TRAFFIC_SOURCES) -> str:
-    """sha256 over the kernel sources a traffic record was captured from."""
+def code_of(src: str) -> str:
+    """C/C++/CUDA source without its comments, each line's whitespace runs
+    collapsed and blank lines dropped: what the compiler sees, so an edit to
+    a comment leaves it unchanged and an edit to the code does not."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":  # a string or character literal, copied whole
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    lines = (" ".join(line.split()) for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line)
+
+
+def sources_code_sha256(files=TRAFFIC_SOURCES) -> str:
+    """sha256 over the code (comments stripped) of the kernel sources a
+    traffic record was captured from."""
     hsh = hashlib.sha256()
     for f in files:
-        hsh.update(open(os.path.join(ROOT, "combine_symmetric_heap_gb300", "csrc", f), "rb").read())
+        src = open(os.path.join(ROOT, "combine_symmetric_heap_gb300", "csrc", f), encoding="utf-8").read()
+        hsh.update(code_of(src).encode())
     return hsh.hexdigest()
 
 
 def traffic_record(workload: str, cfg: dict):
     """Per-step DRAM bytes of the expert FFN launches from the committed ncu
-    summary, or None if it was captured for another workload or shape, or any
-    of its sources changed since."""
+    summary, or None if it was captured for another workload or shape, or the
+    code of any of its sources changed since."""
     import moe_synth as ms
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
         rec = json.load(open(path))
-        if rec.get("sources_sha256") != sources_sha256():
+        if rec.get("sources_code_sha256") != sources_code_sha256():
             return None
         if rec.get("workload") != workload or cfg != ms.CONFIGS.get(workload):
             return None

@@ -67,7 +67,7 @@ def test_traffic_record_only_for_its_workload():
     rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
     name = rec["workload"]
     cfg = dict(ms.CONFIGS[name])
-    expect = rec["traffic_bytes_per_step"] if rec["sources_sha256"] == bench.sources_sha256() else None
+    expect = rec["traffic_bytes_per_step"] if rec["sources_code_sha256"] == bench.sources_code_sha256() else None
     assert bench.traffic_record(name, cfg) == expect
     other = next(k for k in ms.CONFIGS if k != name)
     assert bench.traffic_record(other, dict(ms.CONFIGS[other])) is None

@@ -72,3 +72,18 @@ def test_clock_summary_keeps_only_the_timed_window():
     c.window = None                                  # no window: every sample counts
     s = c.summary()
     assert s["samples"] == 3 and "sw_thermal_slowdown" in s["reasons"] and s["sm_min_mhz"] == 1500.0
+
+
+def test_code_hash_ignores_comments_only():
+    """The traffic record is keyed to the kernels' code: a comment edit or
+    re-indentation keeps the key, any code edit changes it, and comment
+    markers inside string or character literals are code."""
+    src = ('// header\n#include "x.cuh"\n/* block\n comment */ int f(int a) {\n'
+           '  return a + 1;  // trailing\n}\nconst char *s = "a // b /* c */";\nchar q = \'/\';\n')
+    base = bench.code_of(src)
+    assert "header" not in base and "trailing" not in base and "block" not in base
+    assert '"a // b /* c */"' in base and "'/'" in base
+    assert bench.code_of(src.replace("// trailing", "// other words")) == base
+    assert bench.code_of(src.replace("  return", "\n\n      return")) == base
+    assert bench.code_of(src.replace("a + 1", "a + 2")) != base
+    assert bench.code_of(src.replace('"a // b /* c */"', '"a // b"')) != base
