@@ -28,7 +28,7 @@ METRIC = "MoE dispatch+expert+combine tokens/s on 1 GB300; % HBM / bf16 tensor r
 UNIT = "tokens/s"
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=100)
@@ -56,7 +56,7 @@ def parse():
                    help="skip the record of the other workloads (the default run adds it to the headline line)")
     p.add_argument("--workload", default="moe", choices=["moe", "linear_a2a"],
                    help="linear_a2a: the GEMM + all-to-all workload on the same heap, fused vs split")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 def dist_env():

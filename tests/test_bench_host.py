@@ -87,3 +87,40 @@ def test_code_hash_ignores_comments_only():
     assert bench.code_of(src.replace("  return", "\n\n      return")) == base
     assert bench.code_of(src.replace("a + 1", "a + 2")) != base
     assert bench.code_of(src.replace('"a // b /* c */"', '"a // b"')) != base
+
+
+def _profile_commands():
+    """Every `python bench.py ...` and `python -m pytest ...` command written
+    in the committed ncu summaries (continuation lines joined)."""
+    import glob
+    import re
+    cmds = []
+    for path in sorted(glob.glob(os.path.join(bench.ROOT, "profiles", "*.md"))):
+        text = re.sub(r"\\\n\s*", " ", open(path, encoding="utf-8").read())
+        for line in text.splitlines():
+            for m in re.finditer(r"python (bench\.py|-m pytest)([^`\n]*)", line):
+                cmds.append((os.path.basename(path), m.group(1), m.group(2).strip()))
+    return cmds
+
+
+def test_profile_commands_run_committed_files_with_valid_flags():
+    """The commands the profile summaries give still parse: bench.py accepts
+    every flag they pass and knows every workload they name, and the test
+    files they run exist."""
+    import shlex
+    import moe_synth as ms
+    cmds = _profile_commands()
+    assert len(cmds) >= 10
+    for src, what, rest in cmds:
+        argv = shlex.split(rest)
+        if what == "bench.py":
+            argv = ["deepseek" if a == "NAME" else a for a in argv]
+            args = bench.parse(argv)
+            assert args.config in ms.CONFIGS, (src, rest)
+        else:
+            tests = [a for a in argv if a.startswith("tests/")]
+            assert tests and all(os.path.exists(os.path.join(bench.ROOT, t)) for t in tests), (src, rest)
+            if "-k" in argv:  # every word of the selection names something in the file
+                text = "".join(open(os.path.join(bench.ROOT, t), encoding="utf-8").read() for t in tests)
+                words = [w for w in argv[argv.index("-k") + 1].split() if w not in ("and", "or", "not")]
+                assert all(w in text for w in words), (src, rest)
