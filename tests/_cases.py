@@ -24,6 +24,10 @@ SMALL = {
     "allk": dict(world=1, tokens_per_slot=130, hidden=128, num_experts=8, topk=8, inter=256),
     # k = 1, ~300 rows per expert: two token tiles (256 + ragged) per expert
     "multi": dict(world=1, tokens_per_slot=600, hidden=128, num_experts=2, topk=1, inter=256),
+    # 32 slots (the most the deduplicated dispatch takes), two experts per slot
+    "slots32": dict(world=32, tokens_per_slot=24, hidden=128, num_experts=64, topk=4, inter=128),
+    # 64 slots of one expert each, 8 tokens per slot
+    "slots64": dict(world=64, tokens_per_slot=8, hidden=256, num_experts=64, topk=2, inter=128),
 }
 
 

@@ -45,8 +45,25 @@ def _windows(heap, cfg):
     return out
 
 
-CASES = dict(SMALL)
+# the deduplicated dispatch takes up to 32 slots (one ballot bit per slot)
+CASES = {name: cfg for name, cfg in SMALL.items() if cfg["world"] <= 32}
 CASES["deepseek_small"] = dict(ms.CONFIGS["deepseek"], tokens_per_slot=64)
+
+
+def test_dedup_refuses_more_than_32_slots(sm):
+    cfg = SMALL["slots64"]
+    assert cfg["world"] > 32
+    n, k = cfg["world"] * cfg["tokens_per_slot"], cfg["topk"]
+    heap = sm.SymHeap(cfg, DEV)
+    x = ms.x_torch(cfg, DEV)
+    idx = torch.zeros((n, k), dtype=torch.int32, device=DEV)
+    idx[:, 1] = 1
+    w = torch.full((n, k), 0.5, dtype=torch.float32, device=DEV)
+    with pytest.raises(sm.SymmoeError) as err:
+        heap.dispatch(x, idx, w, dedup=True)
+    assert err.value.code == sm.SYM_EINVAL
+    torch.cuda.synchronize()
+    assert heap.status() == 0
 
 
 @pytest.mark.parametrize("name", list(CASES))
